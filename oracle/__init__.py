@@ -1,0 +1,8 @@
+"""CPU oracle (test infrastructure only; never imported by the product path)."""
+from .qkvp_oracle import *  # noqa: F401,F403
+from .qkvp_oracle import (e4m3_decode, e4m3_encode, scale_of, quantize,  # noqa: F401
+                          quantize_with_scale, dequantize, packed_width,
+                          split_columns, quantize_bank, rope_angles, rope,
+                          rope_inverse, rms_norm, packed_gemm, forward,
+                          norm_rope_backward, epilogue_backward, grad_gemms,
+                          backward, E4M3_MAX)

@@ -1,0 +1,391 @@
+// Host side of the C ABI declared in include/qkvp.h: argument validation,
+// tensor-map encoding, workspace layout and the launch sequence of each call.
+// No call allocates device memory and none synchronises the host, except
+// qkvp_poll_device_status.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.cuh"
+
+using namespace qkvp;
+
+namespace {
+
+uint64_t g_timeout_ns = 2000000000ull;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map: `inner` elements per row (contiguous), `outer` rows, rows
+// `row_bytes` apart.
+bool map2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+           uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over a [d2][d1][d0] row-major tensor.
+bool map3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+           uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t padded_tokens(int T) { return (static_cast<int64_t>(T) + 127) / 128 * 128; }
+
+int check_dims(const qkvp_dims* d) {
+  if (!d) return QKVP_ERR_INVALID_ARGUMENT;
+  if (d->T < 1 || d->D < 1 || d->H < 1 || d->d_qk < 1 || d->d_v < 1) return QKVP_ERR_INVALID_ARGUMENT;
+  if (d->T > (1 << 24)) return QKVP_ERR_UNSUPPORTED;
+  if (d->D % 128 != 0 || d->D > 16384) return QKVP_ERR_UNSUPPORTED;
+  if (d->H > 128) return QKVP_ERR_UNSUPPORTED;
+  if (d->d_qk != 64 && d->d_qk != 96 && d->d_qk != 128) return QKVP_ERR_UNSUPPORTED;
+  if (d->d_v != 128) return QKVP_ERR_UNSUPPORTED;
+  return QKVP_OK;
+}
+
+// Workspace: [status 256 B][x amax partials][dY amax partials][dW partials]
+constexpr size_t kStatusBytes = 256;
+constexpr int kMaxParts = 4096;
+constexpr size_t kPartsBytes = kMaxParts * sizeof(float);
+constexpr int kMaxSplits = 16;
+
+struct DwShape {
+  int bn, m_tiles, n_tiles, kblocks_total;
+};
+DwShape dw_shape(const qkvp_dims* d) {
+  const int N = d->H * (2 * d->d_qk + d->d_v);
+  DwShape s;
+  s.bn = d->D % 256 == 0 ? 256 : 128;
+  s.m_tiles = (N + 127) / 128;
+  s.n_tiles = d->D / s.bn;
+  s.kblocks_total = static_cast<int>(padded_tokens(d->T) / 128);
+  return s;
+}
+size_t dw_partial_bytes(const DwShape& s, int splits) {
+  return static_cast<size_t>(splits) * s.m_tiles * s.n_tiles * s.bn * 128 * sizeof(float);
+}
+size_t ws_bytes_for(const qkvp_dims* d) {
+  return kStatusBytes + 2 * kPartsBytes + dw_partial_bytes(dw_shape(d), kMaxSplits);
+}
+
+// Split count for the dW GEMM: the fewest splits whose units fill the SMs in
+// whole waves to >= 90%, with at least 4 k-blocks per split.
+int choose_splits(int tiles, int kblocks, int sms) {
+  int best = 1;
+  double best_eff = 0.0;
+  const int smax = std::max(1, std::min(kMaxSplits, kblocks / 4));
+  for (int s = 1; s <= smax; ++s) {
+    const int units = tiles * s;
+    const int waves = (units + sms - 1) / sms;
+    const double eff = static_cast<double>(units) / (static_cast<double>(waves) * sms);
+    if (eff >= 0.9) return s;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
+DevStatus dev_status(void* ws) { return DevStatus{static_cast<int*>(ws), g_timeout_ns}; }
+
+#define QKVP_TRY_CUDA(expr)                          \
+  do {                                               \
+    if ((expr) != cudaSuccess) return QKVP_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* qkvp_status_string(int status) {
+  switch (status) {
+    case QKVP_OK: return "QKVP_OK";
+    case QKVP_ERR_INVALID_ARGUMENT: return "QKVP_ERR_INVALID_ARGUMENT";
+    case QKVP_ERR_UNSUPPORTED: return "QKVP_ERR_UNSUPPORTED";
+    case QKVP_ERR_MISALIGNED: return "QKVP_ERR_MISALIGNED";
+    case QKVP_ERR_WORKSPACE_TOO_SMALL: return "QKVP_ERR_WORKSPACE_TOO_SMALL";
+    case QKVP_ERR_CUDA: return "QKVP_ERR_CUDA";
+    case QKVP_ERR_TIMEOUT: return "QKVP_ERR_TIMEOUT";
+    case QKVP_ERR_DEVICE_INPUT: return "QKVP_ERR_DEVICE_INPUT";
+    default: return "QKVP_ERR_UNKNOWN";
+  }
+}
+
+int64_t qkvp_padded_tokens(int T) { return T < 1 ? -1 : padded_tokens(T); }
+
+size_t qkvp_workspace_bytes(const qkvp_dims* dims) {
+  if (check_dims(dims) != QKVP_OK) return 0;
+  return ws_bytes_for(dims);
+}
+
+size_t qkvp_bank_workspace_bytes(int L, int D, int H, int d_qk, int d_v) {
+  const qkvp_dims d{1, D, H, d_qk, d_v};
+  if (L < 1 || L > kMaxLayers || check_dims(&d) != QKVP_OK) return 0;
+  return kStatusBytes + static_cast<size_t>(L) * kBankAmaxBlocks * sizeof(float);
+}
+
+int qkvp_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kStatusBytes) return QKVP_ERR_INVALID_ARGUMENT;
+  QKVP_TRY_CUDA(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+  return QKVP_OK;
+}
+
+int qkvp_poll_device_status(void* ws, int* where, void* stream) {
+  if (!ws) return QKVP_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host[2] = {0, 0};
+  QKVP_TRY_CUDA(cudaMemcpyAsync(host, ws, sizeof(host), cudaMemcpyDeviceToHost, s));
+  QKVP_TRY_CUDA(cudaMemsetAsync(ws, 0, sizeof(host), s));
+  QKVP_TRY_CUDA(cudaStreamSynchronize(s));
+  if (where) *where = host[1];
+  return host[0];
+}
+
+int qkvp_set_wait_timeout_ns(uint64_t ns) {
+  if (ns < 1000000ull || ns > 60000000000ull) return QKVP_ERR_INVALID_ARGUMENT;
+  g_timeout_ns = ns;
+  return QKVP_OK;
+}
+
+int qkvp_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned timeout_us, void* stream) {
+  if (!ws || ws_bytes < kStatusBytes || timeout_us < 1 || timeout_us > 1000000) return QKVP_ERR_INVALID_ARGUMENT;
+  if (!aligned16(ws)) return QKVP_ERR_MISALIGNED;
+  DevStatus st{static_cast<int*>(ws), static_cast<uint64_t>(timeout_us) * 1000ull};
+  QKVP_TRY_CUDA(launch_selftest_wait(st, static_cast<cudaStream_t>(stream)));
+  return QKVP_OK;
+}
+
+int qkvp_build_rope_table(float* table, int max_pos, int d_qk, double base, void* stream) {
+  if (!table || max_pos < 1 || !(base > 1.0)) return QKVP_ERR_INVALID_ARGUMENT;
+  if (d_qk != 64 && d_qk != 96 && d_qk != 128) return QKVP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_pos) * d_qk > (int64_t(1) << 31)) return QKVP_ERR_UNSUPPORTED;
+  if (!aligned16(table)) return QKVP_ERR_MISALIGNED;
+  QKVP_TRY_CUDA(launch_rope_table(table, max_pos, d_qk, base, static_cast<cudaStream_t>(stream)));
+  return QKVP_OK;
+}
+
+int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v, const uint16_t* const* Wq,
+                       const uint16_t* const* Wk, const uint16_t* const* Wv, uint8_t* W8, uint8_t* W8T,
+                       float* w_scale, void* ws, size_t ws_bytes, void* stream) {
+  const qkvp_dims d{1, D, H, d_qk, d_v};
+  if (L < 1 || !Wq || !Wk || !Wv || !W8 || !W8T || !w_scale || !ws) return QKVP_ERR_INVALID_ARGUMENT;
+  const int rc = check_dims(&d);
+  if (rc != QKVP_OK) return rc;
+  if (L > kMaxLayers) return QKVP_ERR_UNSUPPORTED;
+  BankArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int l = 0; l < L; ++l) {
+    if (!Wq[l] || !Wk[l] || !Wv[l]) return QKVP_ERR_INVALID_ARGUMENT;
+    if (!aligned16(Wq[l]) || !aligned16(Wk[l]) || !aligned16(Wv[l])) return QKVP_ERR_MISALIGNED;
+    a.Wq[l] = Wq[l];
+    a.Wk[l] = Wk[l];
+    a.Wv[l] = Wv[l];
+  }
+  if (!aligned16(W8) || !aligned16(W8T) || !aligned16(w_scale) || !aligned16(ws)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < qkvp_bank_workspace_bytes(L, D, H, d_qk, d_v)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  a.W8 = W8;
+  a.W8T = W8T;
+  a.w_scale = w_scale;
+  a.L = L;
+  a.D = D;
+  a.Nq = H * d_qk;
+  a.N = H * (2 * d_qk + d_v);
+  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  QKVP_TRY_CUDA(launch_bank_refresh(a, partials, static_cast<cudaStream_t>(stream)));
+  return QKVP_OK;
+}
+
+int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int max_pos, const uint16_t* x,
+                 const int32_t* pos, const uint8_t* W8, const float* w_scale, uint16_t* q, uint16_t* k,
+                 uint16_t* v, float* rstd, uint8_t* x8, uint8_t* x8T, float* x_scale, void* ws, size_t ws_bytes,
+                 void* stream) {
+  int rc = check_dims(dims);
+  if (rc != QKVP_OK) return rc;
+  if (!rope_table || !x || !pos || !W8 || !w_scale || !q || !k || !v || !rstd || !x8 || !x8T || !x_scale || !ws)
+    return QKVP_ERR_INVALID_ARGUMENT;
+  if (max_pos < 1 || !(eps >= 0.f) || !(eps < 1.f)) return QKVP_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {rope_table, x, pos, W8, w_scale, q, k, v, rstd, x8, x8T, x_scale, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < ws_bytes_for(dims)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return QKVP_ERR_CUDA;
+
+  const int T = dims->T, D = dims->D, H = dims->H, dqk = dims->d_qk, dv = dims->d_v;
+  const int N = H * (2 * dqk + dv);
+  const int64_t Tp = padded_tokens(T);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* xparts = reinterpret_cast<float*>(wsb + kStatusBytes);
+  const DevStatus st = dev_status(ws);
+
+  CUtensorMap tm_x, tm_x8, tm_x8t, tm_w, tm_q, tm_k, tm_v;
+  bool ok = map2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, D, T, D * 2ull, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_x8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8T, Tp, D, Tp, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map3d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!ok) return QKVP_ERR_CUDA;
+
+  const int nparts = std::min(kMaxParts, 4 * sms);
+  QKVP_TRY_CUDA(launch_amax_bf16(x, static_cast<int64_t>(T) * D, xparts, nparts, s));
+  QKVP_TRY_CUDA(launch_x_quant(tm_x, tm_x8, tm_x8t, static_cast<int>(Tp), D, xparts, nparts, x_scale, st, s));
+
+  FwdParams p;
+  p.T = T;
+  p.H = H;
+  p.d_qk = dqk;
+  p.d_v = dv;
+  p.hq = dqk == 64 ? 4 : 2;
+  p.nq = (H + p.hq - 1) / p.hq;
+  p.nv = (H + 1) / 2;
+  p.n_tiles = 2 * p.nq + p.nv;
+  p.num_units = static_cast<int>(Tp / 128) * p.n_tiles;
+  p.kblocks = D / 128;
+  p.eps = eps;
+  p.x_scale = x_scale;
+  p.w_scale = w_scale;
+  p.rope = rope_table;
+  p.max_pos = max_pos;
+  p.pos = pos;
+  p.rstd = rstd;
+  const int grid = std::min(p.num_units, sms);
+  QKVP_TRY_CUDA(launch_fwd_gemm(tm_x8, tm_w, tm_q, tm_k, tm_v, p, grid, st, s));
+  return QKVP_OK;
+}
+
+int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, const uint16_t* dq,
+                  const uint16_t* dk, const uint16_t* dv, const uint16_t* q, const uint16_t* k, const float* rstd,
+                  const int32_t* pos, const uint8_t* W8T, const float* w_scale, const uint8_t* x8T,
+                  const float* x_scale, uint16_t* dx, uint16_t* dW, uint8_t* dY8, uint8_t* dY8T, float* dy_scale,
+                  void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != QKVP_OK) return rc;
+  if (!rope_table || !dq || !dk || !dv || !q || !k || !rstd || !pos || !W8T || !w_scale || !x8T || !x_scale || !dx ||
+      !dW || !dY8 || !dY8T || !dy_scale || !ws)
+    return QKVP_ERR_INVALID_ARGUMENT;
+  if (max_pos < 1) return QKVP_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {rope_table, dq, dk, dv, q, k, rstd, pos, W8T, w_scale, x8T, x_scale, dx, dW, dY8, dY8T,
+                        dy_scale, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < ws_bytes_for(dims)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return QKVP_ERR_CUDA;
+
+  const int T = dims->T, D = dims->D, H = dims->H, dqk = dims->d_qk, dvw = dims->d_v;
+  const int N = H * (2 * dqk + dvw);
+  const int64_t Tp = padded_tokens(T);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* dyparts = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
+  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes);
+  const DevStatus st = dev_status(ws);
+
+  BwdMaps m;
+  bool ok = map3d(&m.dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dq, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&m.dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&m.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, dvw, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map2d(&m.dy8, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && map2d(&m.dy8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8T, Tp, N, Tp, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  CUtensorMap tm_dyA, tm_w8t, tm_dx, tm_dytA, tm_x8tB;
+  ok = ok && map2d(&tm_dyA, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_w8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8T, N, D, N, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dx, D, T, D * 2ull, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map2d(&tm_dytA, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8T, Tp, N, Tp, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_x8tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8T, Tp, D, Tp, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return QKVP_ERR_CUDA;
+
+  BwdParams bp;
+  bp.T = T;
+  bp.H = H;
+  bp.d_qk = dqk;
+  bp.d_v = dvw;
+  bp.N = N;
+  bp.tiles = static_cast<int>(Tp / 128);
+  bp.num_units = bp.tiles * H * 3;
+  bp.rstd = rstd;
+  bp.pos = pos;
+  bp.rope = rope_table;
+  bp.max_pos = max_pos;
+  bp.partials = dyparts;
+  bp.nparts = std::min({bp.num_units, 3 * sms, kMaxParts});
+  bp.dy_scale = dy_scale;
+  QKVP_TRY_CUDA(launch_bwd_amax(m, bp, bp.nparts, st, s));
+  QKVP_TRY_CUDA(launch_bwd_quant(m, bp, std::min(bp.num_units, 2 * sms), st, s));
+
+  DxParams xp;
+  xp.T = T;
+  xp.D = D;
+  xp.bn = D % 256 == 0 ? 256 : 128;
+  xp.n_tiles = D / xp.bn;
+  xp.num_units = bp.tiles * xp.n_tiles;
+  xp.kblocks = (N + 127) / 128;
+  xp.dy_scale = dy_scale;
+  xp.w_scale = w_scale;
+  QKVP_TRY_CUDA(launch_dx_gemm(tm_dyA, tm_w8t, tm_dx, xp, std::min(xp.num_units, sms), st, s));
+
+  const DwShape ds = dw_shape(dims);
+  DwParams wp;
+  wp.N = N;
+  wp.D = D;
+  wp.bn = ds.bn;
+  wp.m_tiles = ds.m_tiles;
+  wp.n_tiles = ds.n_tiles;
+  wp.kblocks_total = ds.kblocks_total;
+  wp.splits = choose_splits(ds.m_tiles * ds.n_tiles, ds.kblocks_total, sms);
+  wp.num_units = wp.splits * ds.m_tiles * ds.n_tiles;
+  wp.partials = dwparts;
+  QKVP_TRY_CUDA(launch_dw_gemm(tm_dytA, tm_x8tB, wp, std::min(wp.num_units, sms), st, s));
+  QKVP_TRY_CUDA(launch_dw_reduce(wp, dy_scale, x_scale, dW, s));
+  return QKVP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,588 @@
+// The three FP8 GEMMs of the packed QKV projection, on 5th-generation tensor
+// cores (tcgen05, kind::f8f6f4, fp32 accumulate in TMEM):
+//   forward  acc = x8 . W8^T        epilogue: de-quantise, split, per-head
+//                                   RMSNorm of q/k, RoPE, head-major bf16 store
+//   dX       acc = dY8 . W8         via W8T (K-major); epilogue: scale, bf16
+//   dW       acc = dY8^T . x8       via dY8T and x8T, split over K (tokens);
+//                                   fp32 partials, reduced in a fixed order
+//
+// One persistent, warp-specialised kernel body serves all three:
+//   warp 0     TMA producer: A tile (128 rows x 128 B of K) and B tile
+//              (ncols rows, loaded as 32-row boxes), 128-byte swizzle
+//   warp 1     TMEM allocator and MMA issuer (one thread): 4 MMAs of K = 32
+//              per stage, commit to the stage's "empty" barrier, and to the
+//              accumulator's "full" barrier after the last stage of a unit
+//   warps 2-5  epilogue, one accumulator row (token) per thread; TMEM holds
+//              two 256-column accumulators so the epilogue of one unit
+//              overlaps the MMAs of the next
+// Every wait is bounded (see mbar_wait); on expiry the kernel records
+// QKVP_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include "kernels.cuh"
+
+namespace qkvp {
+
+constexpr int kBM = 128;                   // accumulator rows (tokens, or bank rows for dW)
+constexpr int kBK = 128;                   // K bytes per stage (E4M3: 128 elements)
+constexpr int kAStage = kBM * kBK;         // 16 KB
+constexpr int kBStage = 256 * kBK;         // 32 KB (largest B tile)
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;             // 2 accumulators x 256 fp32 columns
+constexpr int kEpiWarpBytes = 16384;       // staging per epilogue warp: 8 boxes of 32 x 64 B
+constexpr int kMaxStages = 6;
+
+struct Unit {
+  int a_row, b_row, ncols, kb0, kb1;
+};
+
+struct GemmSmem {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__host__ __device__ constexpr int gemm_smem_bytes(int stages, bool epi_staging) {
+  return 1024 + stages * (kAStage + kBStage) + (epi_staging ? 4 * kEpiWarpBytes : 0);
+}
+
+// ---------------------------------------------------------------------------
+// Producer and MMA roles (one thread each)
+// ---------------------------------------------------------------------------
+template <class Sched>
+__device__ void producer_role(const Sched& sc, const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* sA,
+                              uint8_t* sB, GemmSmem& g, int stages, const DevStatus& st, int kid) {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t used = 0, last_par = 0;  // stages filled at least once; parity of their last fill
+  for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x) {
+    const Unit ui = sc.unit(u);
+    for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+      if (!mbar_wait(&g.empty[stage], phase ^ 1, &g.abort_flag, st, kid)) goto drain;
+      mbar_arrive_expect_tx(&g.full[stage], static_cast<uint32_t>(kAStage + ui.ncols * kBK));
+      tma_load_2d(sA + stage * kAStage, tmA, &g.full[stage], kb * kBK, ui.a_row);
+      for (int j = 0; j < ui.ncols / 32; ++j)
+        tma_load_2d(sB + stage * kBStage + j * 32 * kBK, tmB, &g.full[stage], kb * kBK, ui.b_row + 32 * j);
+      used |= 1u << stage;
+      last_par = (last_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == stages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+  }
+drain:
+  // every copy this thread issued has landed before the CTA may exit
+  for (int s = 0; s < stages; ++s)
+    if (used & (1u << s)) mbar_wait(&g.full[s], (last_par >> s) & 1, nullptr, st, kid);
+}
+
+template <class Sched>
+__device__ void mma_role(const Sched& sc, uint8_t* sA, uint8_t* sB, GemmSmem& g, uint32_t tmem_base, int stages,
+                         const DevStatus& st, int kid) {
+  int stage = 0;
+  uint32_t phase = 0;
+  int it = 0;
+  for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x, ++it) {
+    const Unit ui = sc.unit(u);
+    const int buf = it & 1;
+    const uint32_t use = (it >> 1) & 1;
+    if (!mbar_wait(&g.tempty[buf], use ^ 1, &g.abort_flag, st, kid)) break;
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + buf * 256;
+    const uint32_t idesc = idesc_e4m3_f32(kBM, ui.ncols);
+    bool ok = true;
+    for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+      if (!mbar_wait(&g.full[stage], phase, &g.abort_flag, st, kid)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBStage);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 32; ++kk)
+        umma_e4m3(d_tmem, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
+                  (kb > ui.kb0 || kk > 0) ? 1u : 0u);
+      umma_commit(&g.empty[stage]);
+      if (++stage == stages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    if (!ok) break;
+    umma_commit(&g.tfull[buf]);
+  }
+  // all MMAs issued by this thread have completed before TMEM is freed
+  umma_commit(&g.mma_done);
+  mbar_wait(&g.mma_done, 0, nullptr, st, kid);
+}
+
+// ---------------------------------------------------------------------------
+// Common body
+// ---------------------------------------------------------------------------
+template <class Sched, class Epi>
+__device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUtensorMap* tmA,
+                                          const CUtensorMap* tmB, int stages, const DevStatus& st, int kid) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ GemmSmem g;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + stages * kAStage;
+  uint8_t* sE = sB + stages * kBStage;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    g.abort_flag = 0;
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&g.full[s], 1);
+      mbar_init(&g.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&g.tfull[b], 1);
+      mbar_init(&g.tempty[b], 128);
+    }
+    mbar_init(&g.mma_done, 1);
+    fence_mbar_init();
+    prefetch_tmap(tmA);
+    prefetch_tmap(tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&g.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = g.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) producer_role(sc, tmA, tmB, sA, sB, g, stages, st, kid);
+  } else if (warp == 1) {
+    if (lane == 0) mma_role(sc, sA, sB, g, tmem_base, stages, st, kid);
+  } else {
+    const int qw = warp & 3;  // TMEM lane quarter this warp may access
+    epi.begin(qw, lane, sE + (warp - 2) * kEpiWarpBytes);
+    int it = 0;
+    for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x, ++it) {
+      const int buf = it & 1;
+      if (!mbar_wait(&g.tfull[buf], (it >> 1) & 1, &g.abort_flag, st, kid)) break;
+      tc_fence_after();
+      epi.process(u, tmem_base + static_cast<uint32_t>(buf * 256) + (static_cast<uint32_t>(qw * 32) << 16));
+      tc_fence_before();
+      mbar_arrive(&g.tempty[buf]);
+    }
+    epi.finish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// 16-byte chunk `col / 8` of row `row` in a staging box of 32 rows x 32
+// bf16 columns (64 B rows) with 64-byte swizzling, as TMA reads it.
+__device__ __forceinline__ void stage_chunk_sw64(uint8_t* box, int row, int col_in_box, uint4 v) {
+  const int cc = col_in_box >> 3;
+  *reinterpret_cast<uint4*>(box + row * 64 + ((cc ^ ((row >> 1) & 3)) << 4)) = v;
+}
+
+// Stage 16 consecutive bf16 columns [c0, c0+16) of one row (c0 % 16 == 0)
+// into a group of consecutive 2 KB boxes.
+__device__ __forceinline__ void stage16(uint8_t* boxes, int row, int c0, const uint32_t (&w)[8]) {
+  uint8_t* box = boxes + (c0 >> 5) * 2048;
+  stage_chunk_sw64(box, row, c0 & 31, make_uint4(w[0], w[1], w[2], w[3]));
+  stage_chunk_sw64(box, row, (c0 & 31) + 8, make_uint4(w[4], w[5], w[6], w[7]));
+}
+
+// ---------------------------------------------------------------------------
+// Forward: schedule and epilogue
+// ---------------------------------------------------------------------------
+struct FwdSched {
+  const FwdParams& p;
+  __device__ int num_units() const { return p.num_units; }
+  // kind 0 = q, 1 = k, 2 = v
+  __device__ void decode(int j, int& kind, int& head0, int& nh) const {
+    if (j < p.nq) {
+      kind = 0;
+      head0 = j * p.hq;
+      nh = min(p.hq, p.H - head0);
+    } else if (j < 2 * p.nq) {
+      kind = 1;
+      head0 = (j - p.nq) * p.hq;
+      nh = min(p.hq, p.H - head0);
+    } else {
+      kind = 2;
+      head0 = (j - 2 * p.nq) * 2;
+      nh = min(2, p.H - head0);
+    }
+  }
+  __device__ Unit unit(int u) const {
+    const int m = u / p.n_tiles, j = u % p.n_tiles;
+    int kind, head0, nh;
+    decode(j, kind, head0, nh);
+    Unit r;
+    r.a_row = m * kBM;
+    if (kind == 0) {
+      r.b_row = head0 * p.d_qk;
+      r.ncols = nh * p.d_qk;
+    } else if (kind == 1) {
+      r.b_row = p.H * p.d_qk + head0 * p.d_qk;
+      r.ncols = nh * p.d_qk;
+    } else {
+      r.b_row = 2 * p.H * p.d_qk + head0 * p.d_v;
+      r.ncols = nh * p.d_v;
+    }
+    r.kb0 = 0;
+    r.kb1 = p.kblocks;
+    return r;
+  }
+};
+
+template <int DQK>
+struct FwdEpi {
+  const FwdParams& p;
+  const FwdSched& sc;
+  const CUtensorMap* tq;
+  const CUtensorMap* tk;
+  const CUtensorMap* tv;
+  const DevStatus& st;
+  uint8_t* stage;
+  int qw, lane, half;
+  float sxw;
+
+  __device__ void begin(int qw_, int lane_, uint8_t* stage_) {
+    qw = qw_;
+    lane = lane_;
+    stage = stage_;
+    half = 0;
+    sxw = (*p.x_scale) * (*p.w_scale);
+  }
+  __device__ void finish() {
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  }
+  // wait until the stores that last read staging half `half` are done
+  __device__ uint8_t* acquire_half() {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    return stage + half * 8192;
+  }
+
+  __device__ void process(int u, uint32_t tacc) {
+    constexpr int HALF = DQK / 2;
+    const int m = u / p.n_tiles, j = u % p.n_tiles;
+    int kind, head0, nh;
+    sc.decode(j, kind, head0, nh);
+    const int row = qw * 32 + lane;
+    const int t = m * kBM + row;
+    const int ty = m * kBM + qw * 32;
+    const bool valid = t < p.T;
+    int pos = 0;
+    if (valid && kind < 2) {
+      pos = __ldg(p.pos + t);
+      if (pos < 0 || pos >= p.max_pos) {
+        record_error(st, QKVP_ERR_DEVICE_INPUT, KID_FWD_GEMM);
+        pos = 0;
+      }
+    }
+    const float2* rope = reinterpret_cast<const float2*>(p.rope);
+    for (int hh = 0; hh < nh; ++hh) {
+      const int h = head0 + hh;
+      uint8_t* buf = acquire_half();
+      if (kind < 2) {
+        uint32_t raw[DQK];
+#pragma unroll
+        for (int c = 0; c < DQK / 16; ++c) tmem_ld16(tacc + hh * DQK + 16 * c, raw + 16 * c);
+        tmem_ld_wait();
+        float v[DQK];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < DQK; ++i) {
+          v[i] = __uint_as_float(raw[i]) * sxw;
+          ss = fmaf(v[i], v[i], ss);
+        }
+        const float r = 1.0f / sqrtf(__fdiv_rn(ss, static_cast<float>(DQK)) + p.eps);
+        if (valid) p.rstd[(static_cast<int64_t>(kind) * p.H + h) * p.T + t] = r;
+#pragma unroll
+        for (int g = 0; g < HALF / 16; ++g) {
+          uint32_t lo[8], hi[8];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const int c = g * 16 + i;
+            const float2 cs0 = __ldg(rope + static_cast<int64_t>(c) * p.max_pos + pos);
+            const float2 cs1 = __ldg(rope + static_cast<int64_t>(c + 1) * p.max_pos + pos);
+            const float a0 = v[c] * r, a1 = v[c + 1] * r;
+            const float b0 = v[HALF + c] * r, b1 = v[HALF + c + 1] * r;
+            lo[i / 2] = pack_bf16x2(a0 * cs0.x - b0 * cs0.y, a1 * cs1.x - b1 * cs1.y);
+            hi[i / 2] = pack_bf16x2(b0 * cs0.x + a0 * cs0.y, b1 * cs1.x + a1 * cs1.y);
+          }
+          stage16(buf, lane, g * 16, lo);
+          stage16(buf, lane, HALF + g * 16, hi);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const CUtensorMap* map = kind == 0 ? tq : tk;
+#pragma unroll
+          for (int b = 0; b < DQK / 32; ++b) tma_store_3d(map, buf + b * 2048, 32 * b, ty, h);
+          bulk_commit();
+        }
+      } else {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t raw[64];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld16(tacc + hh * 128 + hf * 64 + 16 * c, raw + 16 * c);
+          tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(raw[g * 16 + 2 * i]) * sxw,
+                                 __uint_as_float(raw[g * 16 + 2 * i + 1]) * sxw);
+            stage16(buf, lane, hf * 64 + g * 16, w);
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) tma_store_3d(tv, buf + b * 2048, 32 * b, ty, h);
+          bulk_commit();
+        }
+      }
+      half ^= 1;
+    }
+  }
+};
+
+template <int DQK>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ FwdParams p, DevStatus st,
+                    int stages) {
+  FwdSched sc{p};
+  FwdEpi<DQK> epi{p, sc, &tq, &tk, &tv, st};
+  gemm_body(sc, epi, &tmA, &tmB, stages, st, KID_FWD_GEMM);
+}
+
+// ---------------------------------------------------------------------------
+// dX: schedule and epilogue
+// ---------------------------------------------------------------------------
+struct DxSched {
+  const DxParams& p;
+  __device__ int num_units() const { return p.num_units; }
+  __device__ Unit unit(int u) const {
+    Unit r;
+    r.a_row = (u / p.n_tiles) * kBM;
+    r.b_row = (u % p.n_tiles) * p.bn;
+    r.ncols = p.bn;
+    r.kb0 = 0;
+    r.kb1 = p.kblocks;
+    return r;
+  }
+};
+
+struct DxEpi {
+  const DxParams& p;
+  const CUtensorMap* tdx;
+  uint8_t* stage;
+  int qw, lane, ring;
+  float sc;
+  __device__ void begin(int qw_, int lane_, uint8_t* stage_) {
+    qw = qw_;
+    lane = lane_;
+    stage = stage_;
+    ring = 0;
+    sc = (*p.dy_scale) * (*p.w_scale);
+  }
+  __device__ void finish() {
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  }
+  __device__ void process(int u, uint32_t tacc) {
+    const int m = u / p.n_tiles, j = u % p.n_tiles;
+    const int ty = m * kBM + qw * 32;
+    for (int c0 = 0; c0 < p.bn; c0 += 32) {
+      uint8_t* slot = stage + (ring & 7) * 2048;
+      if (lane == 0) bulk_wait_read<7>();
+      __syncwarp();
+      uint32_t raw[32];
+      tmem_ld16(tacc + c0, raw);
+      tmem_ld16(tacc + c0 + 16, raw + 16);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(raw[g * 16 + 2 * i]) * sc, __uint_as_float(raw[g * 16 + 2 * i + 1]) * sc);
+        stage16(slot, lane, g * 16, w);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tdx, slot, j * p.bn + c0, ty);
+        bulk_commit();
+      }
+      ++ring;
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tdx, const __grid_constant__ DxParams p, DevStatus st,
+                   int stages) {
+  DxSched sc{p};
+  DxEpi epi{p, &tdx};
+  gemm_body(sc, epi, &tmA, &tmB, stages, st, KID_DX_GEMM);
+}
+
+// ---------------------------------------------------------------------------
+// dW: split-K schedule, fp32 partial epilogue, fixed-order reduction
+// ---------------------------------------------------------------------------
+struct DwSched {
+  const DwParams& p;
+  __device__ int num_units() const { return p.num_units; }
+  __device__ Unit unit(int u) const {
+    const int mn = p.m_tiles * p.n_tiles;
+    const int tile = u % mn, split = u / mn;
+    Unit r;
+    r.a_row = (tile / p.n_tiles) * kBM;
+    r.b_row = (tile % p.n_tiles) * p.bn;
+    r.ncols = p.bn;
+    r.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks_total / p.splits);
+    r.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks_total / p.splits);
+    return r;
+  }
+};
+
+struct DwEpi {
+  const DwParams& p;
+  int qw, lane;
+  __device__ void begin(int qw_, int lane_, uint8_t*) {
+    qw = qw_;
+    lane = lane_;
+  }
+  __device__ void finish() {}
+  __device__ void process(int u, uint32_t tacc) {
+    // unit u owns partials[u][bn][128] (column-major tile): coalesced stores
+    float* dst = p.partials + static_cast<int64_t>(u) * p.bn * kBM + qw * 32 + lane;
+    for (int c0 = 0; c0 < p.bn; c0 += 32) {
+      uint32_t raw[32];
+      tmem_ld16(tacc + c0, raw);
+      tmem_ld16(tacc + c0 + 16, raw + 16);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[static_cast<int64_t>(c0 + i) * kBM] = __uint_as_float(raw[i]);
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dw_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ DwParams p, DevStatus st, int stages) {
+  DwSched sc{p};
+  DwEpi epi{p};
+  gemm_body(sc, epi, &tmA, &tmB, stages, st, KID_DW_GEMM);
+}
+
+// dW[n][d] = bf16(s_dy * s_x * sum over splits, in split order, of the
+// partials).  grid: (m_tiles * n_tiles, bn / 32), 256 threads: thread =
+// (row in tile, 16-column half).
+__global__ void __launch_bounds__(256) dw_reduce_kernel(const __grid_constant__ DwParams p, const float* dy_scale,
+                                                        const float* x_scale, uint16_t* dW) {
+  const int tile = blockIdx.x, c0 = blockIdx.y * 32 + (threadIdx.x >> 7) * 16;
+  const int row = threadIdx.x & 127;
+  const int mn = p.m_tiles * p.n_tiles;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int s = 0; s < p.splits; ++s) {
+    const float* src = p.partials + (static_cast<int64_t>(s * mn + tile) * p.bn + c0) * kBM + row;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] += __ldcs(src + i * kBM);
+  }
+  const int n = (tile / p.n_tiles) * kBM + row;
+  if (n >= p.N) return;
+  const int d = (tile % p.n_tiles) * p.bn + c0;
+  const float sc = (*dy_scale) * (*x_scale);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(acc[2 * i] * sc, acc[2 * i + 1] * sc);
+  uint4* out = reinterpret_cast<uint4*>(dW + static_cast<int64_t>(n) * p.D + d);
+  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+constexpr int kFwdStages = 3, kDxStages = 3, kDwStages = 4;
+
+template <class K>
+static cudaError_t set_smem_once(K kernel, int bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < 64) done[dev] = true;
+  return e;
+}
+
+template <int DQK>
+static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
+                                DevStatus st, cudaStream_t s) {
+  static bool done[64] = {};
+  const int smem = gemm_smem_bytes(kFwdStages, true);
+  cudaError_t e = set_smem_once(fwd_gemm_kernel<DQK>, smem, done);
+  if (e != cudaSuccess) return e;
+  fwd_gemm_kernel<DQK><<<grid, kThreads, smem, s>>>(tmA, tmB, tq, tk, tv, p, st, kFwdStages);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tq,
+                            const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
+                            DevStatus st, cudaStream_t s) {
+  switch (p.d_qk) {
+    case 64: return launch_fwd_t<64>(tmA, tmB, tq, tk, tv, p, grid, st, s);
+    case 96: return launch_fwd_t<96>(tmA, tmB, tq, tk, tv, p, grid, st, s);
+    case 128: return launch_fwd_t<128>(tmA, tmB, tq, tk, tv, p, grid, st, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
+                           const DxParams& p, int grid, DevStatus st, cudaStream_t s) {
+  static bool done[64] = {};
+  const int smem = gemm_smem_bytes(kDxStages, true);
+  cudaError_t e = set_smem_once(dx_gemm_kernel, smem, done);
+  if (e != cudaSuccess) return e;
+  dx_gemm_kernel<<<grid, kThreads, smem, s>>>(tmA, tmB, tdx, p, st, kDxStages);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int grid,
+                           DevStatus st, cudaStream_t s) {
+  static bool done[64] = {};
+  const int smem = gemm_smem_bytes(kDwStages, false);
+  cudaError_t e = set_smem_once(dw_gemm_kernel, smem, done);
+  if (e != cudaSuccess) return e;
+  dw_gemm_kernel<<<grid, kThreads, smem, s>>>(tmA, tmB, p, st, kDwStages);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_reduce(const DwParams& p, const float* dy_scale, const float* x_scale, uint16_t* dW,
+                             cudaStream_t s) {
+  dw_reduce_kernel<<<dim3(p.m_tiles * p.n_tiles, p.bn / 32), 256, 0, s>>>(p, dy_scale, x_scale, dW);
+  return cudaGetLastError();
+}
+
+}  // namespace qkvp

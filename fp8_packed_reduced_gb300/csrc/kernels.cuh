@@ -1,0 +1,101 @@
+// Argument blocks and host-side launchers of the qkvp kernels.  Every
+// launcher enqueues on `stream` and returns the cudaError_t of the launch.
+#pragma once
+
+#include "common.cuh"
+
+namespace qkvp {
+
+constexpr int kMaxLayers = 128;
+
+// ---------------------------------------------------------------------------
+// Bank refresh
+// ---------------------------------------------------------------------------
+struct BankArgs {
+  const uint16_t* Wq[kMaxLayers];
+  const uint16_t* Wk[kMaxLayers];
+  const uint16_t* Wv[kMaxLayers];
+  uint8_t* W8;       // [L, N, D]
+  uint8_t* W8T;      // [L, D, N]
+  float* w_scale;    // [L]
+  int L, D, N, Nq;   // Nq = H * d_qk
+};
+constexpr int kBankAmaxBlocks = 32;   // partial maxima per layer
+
+cudaError_t launch_bank_refresh(const BankArgs& a, float* partials, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Activation quantisation
+// ---------------------------------------------------------------------------
+// amax of n bf16 values at x (16-byte aligned); writes `blocks` partials.
+cudaError_t launch_amax_bf16(const uint16_t* x, int64_t n, float* partials, int blocks, cudaStream_t s);
+// x [T, D] -> x8 [T, D], x8T [D, Tp], x_scale; reads `nparts` partials.
+cudaError_t launch_x_quant(const CUtensorMap& tm_x, const CUtensorMap& tm_x8, const CUtensorMap& tm_x8t, int Tp,
+                           int D, const float* partials, int nparts, float* x_scale, DevStatus st,
+                           cudaStream_t s);
+
+cudaError_t launch_rope_table(float* table, int max_pos, int d_qk, double base, cudaStream_t s);
+cudaError_t launch_selftest_wait(DevStatus st, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// GEMMs (tcgen05, M = 128 tiles, K-major E4M3 operands via TMA)
+// ---------------------------------------------------------------------------
+struct FwdParams {
+  int T, H, d_qk, d_v;
+  int hq;            // heads per Q (or K) tile
+  int nq;            // Q tiles (= K tiles) per 128-token block
+  int nv;            // V tiles per block (2 heads each)
+  int n_tiles;       // 2*nq + nv
+  int num_units;     // ceil(T/128) * n_tiles
+  int kblocks;       // D / 128
+  float eps;
+  const float* x_scale;
+  const float* w_scale;
+  const float* rope;  // [d_qk/2][max_pos] (cos, sin)
+  int max_pos;
+  const int32_t* pos;
+  float* rstd;        // [2, H, T]
+};
+
+struct DxParams {
+  int T, D, bn, n_tiles, num_units, kblocks;
+  const float* dy_scale;
+  const float* w_scale;
+};
+
+struct DwParams {
+  int N, D, bn, m_tiles, n_tiles, splits, num_units, kblocks_total;
+  float* partials;    // [splits][m_tiles][n_tiles][bn][128] float32
+};
+
+cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tq,
+                            const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
+                            DevStatus st, cudaStream_t s);
+cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
+                           const DxParams& p, int grid, DevStatus st, cudaStream_t s);
+cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int grid,
+                           DevStatus st, cudaStream_t s);
+cudaError_t launch_dw_reduce(const DwParams& p, const float* dy_scale, const float* x_scale, uint16_t* dW,
+                             cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Backward epilogue (norm/RoPE backward, dY amax, dY quantisation)
+// ---------------------------------------------------------------------------
+struct BwdParams {
+  int T, H, d_qk, d_v, N, tiles, num_units;
+  const float* rstd;     // [2, H, T]
+  const int32_t* pos;
+  const float* rope;
+  int max_pos;
+  float* partials;       // amax partials (written by pass 1, read by pass 2)
+  int nparts;            // grid of pass 1
+  float* dy_scale;       // written by pass 2
+};
+struct BwdMaps {
+  CUtensorMap dq, q, dk, k, dv;   // loads, 3-D [H][T][d], box {32, 128, 1}, 64-byte swizzle
+  CUtensorMap dy8, dy8t;          // stores: [T][N] box {32, 128}; [N][Tp] box {128, 32} 128-byte swizzle
+};
+cudaError_t launch_bwd_amax(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s);
+cudaError_t launch_bwd_quant(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s);
+
+}  // namespace qkvp

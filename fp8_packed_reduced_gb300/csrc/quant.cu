@@ -1,0 +1,283 @@
+// Bandwidth-bound quantisation kernels:
+//   bank refresh  (amax per layer, then codes in both layouts from one pass)
+//   x amax        (per-tensor amax of the activations)
+//   x quantise    (codes of x in token-major and token-minor layouts, one read)
+//   RoPE table, and the timeout self-test kernel.
+#include "kernels.cuh"
+
+namespace qkvp {
+
+// ---------------------------------------------------------------------------
+// Per-tensor amax of a bf16 tensor: one partial maximum per block.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float absmax_bf16x8(uint4 w) {
+  float m = 0.f;
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, fabsf(bf16_lo(u[i])));
+    m = fmaxf(m, fabsf(bf16_hi(u[i])));
+  }
+  return m;
+}
+
+// x: n16 groups of 8 bf16 (16 bytes) followed by `tail` (< 8) bf16 values.
+__global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restrict__ x, int64_t n16, int tail,
+                                                         float* __restrict__ partials) {
+  __shared__ float red[32];
+  const uint4* p = reinterpret_cast<const uint4*>(x);
+  float m = 0.f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {  // four independent loads in flight
+    const uint4 a = __ldg(p + i), b = __ldg(p + i + stride), c = __ldg(p + i + 2 * stride),
+                d = __ldg(p + i + 3 * stride);
+    m = fmaxf(m, fmaxf(fmaxf(absmax_bf16x8(a), absmax_bf16x8(b)), fmaxf(absmax_bf16x8(c), absmax_bf16x8(d))));
+  }
+  for (; i < n16; i += stride) m = fmaxf(m, absmax_bf16x8(__ldg(p + i)));
+  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail)
+    m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(x[n16 * 8 + threadIdx.x]) << 16)));
+  m = block_max(m, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
+cudaError_t launch_amax_bf16(const uint16_t* x, int64_t n, float* partials, int blocks, cudaStream_t s) {
+  amax_bf16_kernel<<<blocks, 256, 0, s>>>(x, n / 8, static_cast<int>(n % 8), partials);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Bank refresh.  Pass 1: amax of each layer's logical Q/K/V packs, read in
+// place (no concatenation).  Pass 2: every block re-reduces its layer's
+// partials, then converts a 128 x 128 tile of the bank and writes it to both
+// W8 (row-major) and W8T (transposed) from the one read of that tile.  All
+// layers of a refresh go in one launch per pass; the second pass reads the
+// bank back from L2 for bank sizes that fit there.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ const uint16_t* bank_row(const BankArgs& a, int l, int n) {
+  if (n < a.Nq) return a.Wq[l] + static_cast<int64_t>(n) * a.D;
+  if (n < 2 * a.Nq) return a.Wk[l] + static_cast<int64_t>(n - a.Nq) * a.D;
+  return a.Wv[l] + static_cast<int64_t>(n - 2 * a.Nq) * a.D;
+}
+
+// grid: (kBankAmaxBlocks, L), 256 threads.
+__global__ void __launch_bounds__(256) bank_amax_kernel(const __grid_constant__ BankArgs a, float* partials) {
+  __shared__ float red[32];
+  const int l = blockIdx.y;
+  const int row_chunks = a.D / 8;  // 16-byte chunks per row
+  const int64_t total = static_cast<int64_t>(a.N) * row_chunks;
+  float m = 0.f;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / row_chunks), c = static_cast<int>(i % row_chunks);
+    m = fmaxf(m, absmax_bf16x8(__ldg(reinterpret_cast<const uint4*>(bank_row(a, l, n)) + c)));
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) partials[l * gridDim.x + blockIdx.x] = m;
+}
+
+// grid: (ceil(N/128) * D/128, L); 256 threads; tile 128 rows x 128 columns.
+__global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__ BankArgs a,
+                                                         const float* partials) {
+  __shared__ float red[32];
+  __shared__ __align__(16) uint8_t tr[128][128 + 16];  // [column][row] codes
+  const int l = blockIdx.y;
+  const int tiles_d = a.D / 128;
+  const int n0 = (blockIdx.x / tiles_d) * 128, d0 = (blockIdx.x % tiles_d) * 128;
+  const float amax = block_reduce_partials(partials + l * kBankAmaxBlocks, kBankAmaxBlocks, red);
+  const float s = scale_from_amax(amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.w_scale[l] = s;
+
+  const int r = threadIdx.x >> 1;          // tile row
+  const int ch = (threadIdx.x & 1) * 64;   // first of this thread's 64 columns
+  const int n = n0 + r;
+  uint8_t* W8 = a.W8 + static_cast<int64_t>(l) * a.N * a.D;
+  uint8_t* W8T = a.W8T + static_cast<int64_t>(l) * a.N * a.D;
+  if (n < a.N) {
+    const uint4* src = reinterpret_cast<const uint4*>(bank_row(a, l, n) + d0 + ch);
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __ldg(src + j);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const uint32_t w[8] = {v[j].x, v[j].y, v[j].z, v[j].w, v[j + 1].x, v[j + 1].y, v[j + 1].z, v[j + 1].w};
+      uint32_t c[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        c[q] = quant4(bf16_lo(w[2 * q]), bf16_hi(w[2 * q]), bf16_lo(w[2 * q + 1]), bf16_hi(w[2 * q + 1]), s);
+      *reinterpret_cast<uint4*>(W8 + static_cast<int64_t>(n) * a.D + d0 + ch + j * 8) =
+          make_uint4(c[0], c[1], c[2], c[3]);
+#pragma unroll
+      for (int b = 0; b < 16; ++b) tr[ch + j * 8 + b][r] = static_cast<uint8_t>(c[b >> 2] >> (8 * (b & 3)));
+    }
+  } else {
+#pragma unroll 1
+    for (int b = 0; b < 64; ++b) tr[ch + b][r] = 0;
+  }
+  __syncthreads();
+  // W8T rows d0..d0+127, columns n0..n0+127 (clipped at N); 16 bytes per step.
+  const int nvalid = min(128, a.N - n0);
+  for (int i = threadIdx.x; i < 128 * 8; i += 256) {
+    const int col = i >> 3, part = (i & 7) * 16;
+    if (part < nvalid) {
+      const uint4 val = *reinterpret_cast<const uint4*>(&tr[col][part]);
+      uint8_t* dst = W8T + static_cast<int64_t>(d0 + col) * a.N + n0 + part;
+      if (part + 16 <= nvalid) {
+        *reinterpret_cast<uint4*>(dst) = val;
+      } else {
+        const uint8_t* b = reinterpret_cast<const uint8_t*>(&val);
+        for (int q = 0; q < nvalid - part; ++q) dst[q] = b[q];
+      }
+    }
+  }
+}
+
+cudaError_t launch_bank_refresh(const BankArgs& a, float* partials, cudaStream_t s) {
+  bank_amax_kernel<<<dim3(kBankAmaxBlocks, a.L), 256, 0, s>>>(a, partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int tiles = ((a.N + 127) / 128) * (a.D / 128);
+  bank_quant_kernel<<<dim3(tiles, a.L), 256, 0, s>>>(a, partials);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// x -> x8 [T, D] and x8T [D, Tp] from one read.  Tile: 128 tokens x 128
+// columns, loaded by TMA as two 64-column boxes with 128-byte swizzling.
+// Each thread owns one token row: it reads its 128 values without bank
+// conflicts, writes 128 codes into the token-major staging tile (128-byte
+// swizzle) and one byte per column into the column-major staging tile.  Both
+// tiles leave by TMA.  Rows past T are zero-filled by TMA and so produce zero
+// codes in the padding columns of x8T; the x8 store is clipped at T.
+// grid: (Tp/128, D/128), 128 threads.
+// ---------------------------------------------------------------------------
+constexpr int kXQuantSmem = 1024 + 32768 + 16384 + 16384;
+
+__global__ void __launch_bounds__(128) x_quant_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                      const __grid_constant__ CUtensorMap tm_x8,
+                                                      const __grid_constant__ CUtensorMap tm_x8t,
+                                                      const float* partials, int nparts, float* x_scale,
+                                                      DevStatus st) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sx = smem;            // 2 x 16 KB: bf16 [128 rows][64 cols], 128-byte swizzle
+  uint8_t* s8 = smem + 32768;    // 16 KB: codes [128 tokens][128 cols], 128-byte swizzle
+  uint8_t* s8t = smem + 49152;   // 16 KB: codes [128 cols][128 tokens], 128-byte swizzle
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ float red[32];
+  __shared__ int abort_flag;
+
+  const int t0 = blockIdx.x * 128, d0 = blockIdx.y * 128;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar, 32768);
+    tma_load_2d(sx, &tm_x, &bar, d0, t0);
+    tma_load_2d(sx + 16384, &tm_x, &bar, d0 + 64, t0);
+  }
+  const float amax = block_reduce_partials(partials, nparts, red);
+  const float s = scale_from_amax(amax);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *x_scale = s;
+  const bool ok = mbar_wait(&bar, 0, &abort_flag, st, KID_X_QUANT);
+
+  const int r = threadIdx.x;
+  if (ok) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const uint8_t* rowp = sx + half * 16384 + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; c += 2) {  // two 16-byte chunks = 16 values = 16 codes
+        const uint4 u0 = *reinterpret_cast<const uint4*>(rowp + ((c ^ (r & 7)) << 4));
+        const uint4 u1 = *reinterpret_cast<const uint4*>(rowp + (((c + 1) ^ (r & 7)) << 4));
+        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          q[j] = quant4(bf16_lo(w[2 * j]), bf16_hi(w[2 * j]), bf16_lo(w[2 * j + 1]), bf16_hi(w[2 * j + 1]), s);
+        const int col0 = half * 64 + c * 8;  // first column of these 16 codes
+        const int chunk = col0 >> 4;         // 16-byte chunk of the code row
+        *reinterpret_cast<uint4*>(s8 + r * 128 + ((chunk ^ (r & 7)) << 4)) = make_uint4(q[0], q[1], q[2], q[3]);
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+          const int col = col0 + b;
+          s8t[col * 128 + (((r >> 4) ^ (col & 7)) << 4) + (r & 15)] =
+              static_cast<uint8_t>(q[b >> 2] >> (8 * (b & 3)));
+        }
+      }
+    }
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0 && ok) {
+    tma_store_2d(&tm_x8, s8, d0, t0);
+    tma_store_2d(&tm_x8t, s8t, t0, d0);
+    bulk_commit();
+    bulk_wait_all<0>();
+  }
+}
+
+cudaError_t launch_x_quant(const CUtensorMap& tm_x, const CUtensorMap& tm_x8, const CUtensorMap& tm_x8t, int Tp,
+                           int D, const float* partials, int nparts, float* x_scale, DevStatus st,
+                           cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(x_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXQuantSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  x_quant_kernel<<<dim3(Tp / 128, D / 128), 128, kXQuantSmem, s>>>(tm_x, tm_x8, tm_x8t, partials, nparts,
+                                                                   x_scale, st);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RoPE table: table[(i * max_pos + p) * 2 + {0, 1}] = cos, sin of p * w_i.
+// ---------------------------------------------------------------------------
+__global__ void rope_table_kernel(float* table, int max_pos, int half, int d_qk, double base) {
+  const int64_t n = static_cast<int64_t>(half) * max_pos;
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n;
+       j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(j / max_pos), p = static_cast<int>(j % max_pos);
+    const double w = pow(base, -2.0 * i / d_qk);
+    double sn, cs;
+    sincos(static_cast<double>(p) * w, &sn, &cs);
+    table[2 * j] = static_cast<float>(cs);
+    table[2 * j + 1] = static_cast<float>(sn);
+  }
+}
+
+cudaError_t launch_rope_table(float* table, int max_pos, int d_qk, double base, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(d_qk / 2) * max_pos;
+  const int blocks = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  rope_table_kernel<<<blocks, 256, 0, s>>>(table, max_pos, d_qk / 2, d_qk, base);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the failure path: wait on a barrier nothing arrives on.
+// ---------------------------------------------------------------------------
+__global__ void selftest_wait_kernel(DevStatus st) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, st, KID_SELFTEST);
+  __syncthreads();
+}
+
+cudaError_t launch_selftest_wait(DevStatus st, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(st);
+  return cudaGetLastError();
+}
+
+}  // namespace qkvp

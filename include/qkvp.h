@@ -1,0 +1,189 @@
+/*
+ * qkvp.h - C ABI of the reduced-width packed FP8 QKV projection (sm_103a).
+ *
+ * The operation is the attention-input projection described in
+ *   "96 is enough: shrinking attention's routing vectors", section "The change":
+ *       W_packed = concat([W_q, W_k, W_v], dim=out)      (96 + 96 + 128 = 320 cols/head)
+ *       qkv      = fp8_matmul(x, W_packed)
+ *       q, k, v  = split(qkv, [d_qk, d_qk, d_v])
+ *       q, k     = rms_norm(q), rms_norm(k)
+ *       q, k     = rope(q), rope(k)
+ * and in "Track 1 (1.167 min on 8xH100, -5.15% same-node): Reduced-width QK and
+ * packed FP8 attention", section "Changes" (one FP8 operation for packed QKV;
+ * row-major and transposed FP8 bank cached once per optimizer update from one
+ * weight read; norm, RoPE and layout conversion fused; FP8 backward).
+ *
+ * Conventions shared by every call
+ *   - bf16 tensors are passed as uint16_t bit patterns; FP8 tensors as uint8_t
+ *     OCP E4M3FN codes; scales as float32 on the device.
+ *   - All tensor pointers are DEVICE pointers, owned by the caller; the
+ *     library never allocates device memory.  Pointers to arrays of device
+ *     pointers (qkvp_quantize_bank) are HOST arrays.
+ *   - Every tensor pointer must be 16-byte aligned and row-major/contiguous in
+ *     the layout stated at its argument.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream and never synchronise with the host, except
+ *     qkvp_poll_device_status.
+ *   - Arguments are validated on the host before anything is launched; on
+ *     failure nothing is launched and a qkvp_status other than QKVP_OK is
+ *     returned.  No C++ exception crosses this ABI.
+ *   - Errors found on the device (a position outside the RoPE table, a
+ *     device-side wait that ran out of time) are recorded in the status word
+ *     at the start of the workspace and read back by qkvp_poll_device_status.
+ *   - Quantisation: per-tensor scale s = amax / 448 in float32 (s = 1 when
+ *     amax == 0); code = round-to-nearest-even(v / s) onto E4M3FN with
+ *     float32 IEEE division, saturating to +-448.
+ *
+ * Shapes: T tokens, D model width (multiple of 128), H heads, d_qk in
+ * {64, 96, 128}, d_v = 128, N = H * (2*d_qk + d_v) packed rows.
+ * Tp = qkvp_padded_tokens(T) (T rounded up to 128) is the leading dimension
+ * of the token-minor FP8 layouts.
+ */
+#ifndef QKVP_H_
+#define QKVP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qkvp_status {
+    QKVP_OK = 0,
+    QKVP_ERR_INVALID_ARGUMENT = 1,   /* null pointer, non-positive size, bad eps/base     */
+    QKVP_ERR_UNSUPPORTED = 2,        /* shape outside the supported set (see above)       */
+    QKVP_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned                 */
+    QKVP_ERR_WORKSPACE_TOO_SMALL = 4,/* ws_bytes below the size the call needs           */
+    QKVP_ERR_CUDA = 5,               /* a CUDA runtime/driver call or a launch failed    */
+    QKVP_ERR_TIMEOUT = 6,            /* device: a bounded wait expired (status word)     */
+    QKVP_ERR_DEVICE_INPUT = 7        /* device: a position outside [0, max_pos)          */
+} qkvp_status;
+
+typedef struct qkvp_dims {
+    int T;      /* tokens (rows of x), 1 .. 2^24                 */
+    int D;      /* model width, multiple of 128, 128 .. 16384   */
+    int H;      /* heads, 1 .. 128                               */
+    int d_qk;   /* Q/K head width: 64, 96 or 128                 */
+    int d_v;    /* V head width: 128                             */
+} qkvp_dims;
+
+/* Human-readable name of a qkvp_status value (static string, never NULL). */
+const char* qkvp_status_string(int status);
+
+/* T rounded up to a multiple of 128: the leading dimension of x8T and dY8T,
+ * whose padding columns [T, Tp) the library fills with zero codes.  -1 if
+ * T < 1. */
+int64_t qkvp_padded_tokens(int T);
+
+/* Bytes of scratch that qkvp_forward and qkvp_backward need for `dims`
+ * (one workspace serves both).  0 if dims are unsupported.  The workspace
+ * starts with the device status word; zero it once with
+ * qkvp_workspace_init before first use. */
+size_t qkvp_workspace_bytes(const qkvp_dims* dims);
+
+/* Bytes of scratch that qkvp_quantize_bank needs for L layers (0 if the
+ * shape is unsupported). */
+size_t qkvp_bank_workspace_bytes(int L, int D, int H, int d_qk, int d_v);
+
+/* Zero a workspace (status word and all partial buffers).  ws: device. */
+int qkvp_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Read and clear the device status word at the start of `ws`.  Synchronises
+ * `stream`.  Returns QKVP_OK, QKVP_ERR_TIMEOUT or QKVP_ERR_DEVICE_INPUT (the
+ * first error recorded since the last poll), or QKVP_ERR_CUDA if the copy
+ * failed.  If `where` is non-NULL it receives the id of the kernel that
+ * recorded the error (0 when none). */
+int qkvp_poll_device_status(void* ws, int* where, void* stream);
+
+/* RoPE table: table[(i * max_pos + p) * 2 + {0, 1}] = cos, sin of p * w_i,
+ * w_i = base^(-2 i / d_qk), i < d_qk/2, 0 <= p < max_pos, computed in float64
+ * on the device and stored as float32 ("96 is enough", section "The change":
+ * q, k = rope(q), rope(k); rotate-half form).
+ *   table: device, d_qk/2 * max_pos * 2 floats. */
+int qkvp_build_rope_table(float* table, int max_pos, int d_qk, double base, void* stream);
+
+/* Bank refresh, once per optimizer update ("Track 1 ... packed FP8 attention",
+ * section "Changes": row-major and transposed FP8 weight layouts emitted from
+ * a single weight read; the logical Q/K/V packs are quantised without
+ * materialising their concatenation).
+ *   L            layers (1..128)
+ *   Wq, Wk, Wv   HOST arrays of L device pointers to bf16 [H*d_qk, D],
+ *                [H*d_qk, D], [H*d_v, D] (row-major, out x in)
+ *   W8           out, device, [L, N, D] codes; row n of layer l is row n of
+ *                concat(W_q, W_k, W_v)
+ *   W8T          out, device, [L, D, N] codes, W8T[l] = transpose(W8[l])
+ *   w_scale      out, device, [L] float32, one scale per layer (whole bank)
+ *   ws           device scratch of qkvp_bank_workspace_bytes(...) bytes      */
+int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v,
+                       const uint16_t* const* Wq, const uint16_t* const* Wk,
+                       const uint16_t* const* Wv,
+                       uint8_t* W8, uint8_t* W8T, float* w_scale,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Forward ("96 is enough", section "The change"): x is quantised with its own
+ * scale, one FP8 GEMM x8 . W8^T (fp32 accumulate) gives the packed columns,
+ * and its epilogue de-quantises, splits, RMS-normalises q and k per head
+ * (eps inside the square root, no gain), applies rotate-half RoPE at pos[t]
+ * and writes head-major bf16.
+ *   x         in  [T, D] bf16
+ *   pos       in  [T] int32, position of each token inside its sequence
+ *   rope_table,max_pos  from qkvp_build_rope_table(d_qk)
+ *   W8,w_scale in  one layer of qkvp_quantize_bank: [N, D] codes, [1] float
+ *   q, k      out [H, T, d_qk] bf16
+ *   v         out [H, T, d_v] bf16
+ *   rstd      out [2, H, T] float32: 1/sqrt(mean(Y^2)+eps) of q (0) and k (1)
+ *   x8        out [T, D] codes (the GEMM operand)
+ *   x8T       out [D, Tp] codes, transpose of x8, zero in columns >= T
+ *               (saved for the dW GEMM of the backward)
+ *   x_scale   out [1] float32
+ *   ws        scratch, qkvp_workspace_bytes(dims) bytes                    */
+int qkvp_forward(const qkvp_dims* dims, float eps,
+                 const float* rope_table, int max_pos,
+                 const uint16_t* x, const int32_t* pos,
+                 const uint8_t* W8, const float* w_scale,
+                 uint16_t* q, uint16_t* k, uint16_t* v, float* rstd,
+                 uint8_t* x8, uint8_t* x8T, float* x_scale,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of the forward above ("Track 1 ... packed FP8 attention", sections
+ * "Changes" and "Speed": FP8 backward using the cached transposed bank).
+ * y is rebuilt from the saved outputs, y = RoPE^T(q), and
+ * dY_q = rstd * RoPE^T(dq - q * mean(dq * q)) (the same for k), dY_v = dv;
+ * dY is quantised with its own scale into dY8/dY8T, then
+ *   dx = (dY8 . W8) * s_dy * s_w   via W8T as the K-major operand
+ *   dW = (dY8^T . x8) * s_dy * s_x via dY8T and x8T
+ *   dq, dk    in  [H, T, d_qk] bf16     dv in [H, T, d_v] bf16
+ *   q, k      in  [H, T, d_qk] bf16 saved forward outputs
+ *   rstd      in  [2, H, T] float32 saved forward output
+ *   W8T       in  [D, N] codes of the layer, w_scale [1]
+ *   x8T       in  [D, Tp] codes from the forward, x_scale [1]
+ *   dx        out [T, D] bf16           dW out [N, D] bf16 (overwritten)
+ *   dY8       out [T, N] codes          dY8T out [N, Tp] codes (zero cols >= T)
+ *   dy_scale  out [1] float32
+ *   ws        scratch, qkvp_workspace_bytes(dims) bytes                    */
+int qkvp_backward(const qkvp_dims* dims,
+                  const float* rope_table, int max_pos,
+                  const uint16_t* dq, const uint16_t* dk, const uint16_t* dv,
+                  const uint16_t* q, const uint16_t* k, const float* rstd,
+                  const int32_t* pos,
+                  const uint8_t* W8T, const float* w_scale,
+                  const uint8_t* x8T, const float* x_scale,
+                  uint16_t* dx, uint16_t* dW,
+                  uint8_t* dY8, uint8_t* dY8T, float* dy_scale,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* Diagnostic: launch one kernel that waits on a device barrier nothing ever
+ * arrives on, with a wait limit of `timeout_us` microseconds (1..10^6).  The
+ * wait expires, the kernel records QKVP_ERR_TIMEOUT in the status word of
+ * `ws` and returns; the CUDA context stays usable.  Used to test the
+ * failure-reporting path without faulting a GPU. */
+int qkvp_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned timeout_us, void* stream);
+
+/* Device-side wait limit used by every kernel (default 2 s, 1 ms .. 60 s). */
+int qkvp_set_wait_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QKVP_H_ */

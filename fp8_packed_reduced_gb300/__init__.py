@@ -1,0 +1,318 @@
+"""Reduced-width packed FP8 QKV projection for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libqkvp.so`` (declared in
+``include/qkvp.h``).  This module only marshals arguments: it allocates the
+output tensors with torch, passes raw device pointers and the current CUDA
+stream, and turns status codes into exceptions.  Every step of the forward and
+backward runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback, and every call raises if the library is missing.
+
+The method: "96 is enough: shrinking attention's routing vectors", section
+"The change" (packed projection, split, QK RMSNorm, RoPE) and "Track 1
+(1.167 min on 8xH100, -5.15% same-node): Reduced-width QK and packed FP8
+attention", section "Changes" (one FP8 GEMM, dual-layout FP8 bank cached per
+optimizer update, fused norm/RoPE/layout, FP8 backward).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqkvp.so")
+
+STATUS = {
+    0: "QKVP_OK", 1: "QKVP_ERR_INVALID_ARGUMENT", 2: "QKVP_ERR_UNSUPPORTED", 3: "QKVP_ERR_MISALIGNED",
+    4: "QKVP_ERR_WORKSPACE_TOO_SMALL", 5: "QKVP_ERR_CUDA", 6: "QKVP_ERR_TIMEOUT", 7: "QKVP_ERR_DEVICE_INPUT",
+}
+OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_MISALIGNED = 0, 1, 2, 3
+ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_INPUT = 4, 5, 6, 7
+
+
+class QKVPError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("D", ctypes.c_int), ("H", ctypes.c_int),
+                ("d_qk", ctypes.c_int), ("d_v", ctypes.c_int)]
+
+
+_lib_handle = None
+_P = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libqkvp.so; raises if it has not been built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with fp8_packed_reduced_gb300.build.build()"
+                               " (or __graft_entry__.build()); there is no fallback path")
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "qkvp_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "qkvp_padded_tokens": (ctypes.c_int64, [ctypes.c_int]),
+            "qkvp_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Dims)]),
+            "qkvp_bank_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 5),
+            "qkvp_workspace_init": (ctypes.c_int, [_P, ctypes.c_size_t, _P]),
+            "qkvp_poll_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int), _P]),
+            "qkvp_build_rope_table": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_double, _P]),
+            "qkvp_quantize_bank": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.POINTER(_P)] * 3 + [_P] * 4
+                                   + [ctypes.c_size_t, _P]),
+            "qkvp_forward": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_float, _P, ctypes.c_int] + [_P] * 12
+                             + [ctypes.c_size_t, _P]),
+            "qkvp_backward": (ctypes.c_int, [ctypes.POINTER(Dims), _P, ctypes.c_int] + [_P] * 18
+                              + [ctypes.c_size_t, _P]),
+            "qkvp_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint, _P]),
+            "qkvp_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib_handle = L
+    return _lib_handle
+
+
+def _check(code: int, where: str):
+    if code != OK:
+        raise QKVPError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need_cuda(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ----------------------------------------------------------------------------
+# Shapes and scratch
+# ----------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class Shape:
+    T: int
+    D: int
+    H: int
+    d_qk: int = 96
+    d_v: int = 128
+
+    @property
+    def N(self) -> int:
+        return self.H * (2 * self.d_qk + self.d_v)
+
+    @property
+    def Tp(self) -> int:
+        return padded_tokens(self.T)
+
+    def dims(self) -> Dims:
+        return Dims(self.T, self.D, self.H, self.d_qk, self.d_v)
+
+
+def padded_tokens(T: int) -> int:
+    return int(lib().qkvp_padded_tokens(T))
+
+
+def workspace_bytes(shape: Shape) -> int:
+    d = shape.dims()
+    return int(lib().qkvp_workspace_bytes(ctypes.byref(d)))
+
+
+def new_workspace(shape: Shape, device="cuda") -> torch.Tensor:
+    """A zero-initialised workspace for forward/backward of ``shape``."""
+    n = workspace_bytes(shape)
+    if n == 0:
+        raise QKVPError(ERR_UNSUPPORTED, "workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(lib().qkvp_workspace_init(_ptr(ws), n, _stream(ws.device)), "qkvp_workspace_init")
+    return ws
+
+
+def poll_device_status(ws: torch.Tensor):
+    """(status, kernel id) recorded on the device since the last poll; clears it."""
+    where = ctypes.c_int(0)
+    code = lib().qkvp_poll_device_status(_ptr(ws), ctypes.byref(where), _stream(ws.device))
+    return int(code), int(where.value)
+
+
+def set_wait_timeout_ns(ns: int):
+    _check(lib().qkvp_set_wait_timeout_ns(ns), "qkvp_set_wait_timeout_ns")
+
+
+def selftest_wait_timeout(ws: torch.Tensor, timeout_us: int):
+    _check(lib().qkvp_selftest_wait_timeout(_ptr(ws), ws.numel(), timeout_us, _stream(ws.device)),
+           "qkvp_selftest_wait_timeout")
+
+
+def build_rope_table(max_pos: int, d_qk: int, base: float = 10000.0, device="cuda") -> torch.Tensor:
+    """cos/sin table [d_qk/2, max_pos, 2] float32 for RoPE."""
+    t = torch.empty((d_qk // 2, max_pos, 2), dtype=torch.float32, device=device)
+    _check(lib().qkvp_build_rope_table(_ptr(t), max_pos, d_qk, base, _stream(t.device)), "qkvp_build_rope_table")
+    return t
+
+
+# ----------------------------------------------------------------------------
+# Bank refresh (once per optimizer update)
+# ----------------------------------------------------------------------------
+
+def quantize_bank(layers: Sequence[Sequence[torch.Tensor]], H: int, d_qk: int = 96, d_v: int = 128,
+                  out=None):
+    """Quantise L layers of (W_q, W_k, W_v) bf16 into the dual-layout FP8 bank.
+
+    Returns (W8 [L, N, D] uint8, W8T [L, D, N] uint8, w_scale [L] float32).
+    """
+    L = len(layers)
+    D = layers[0][0].shape[1]
+    dev = layers[0][0].device
+    N = H * (2 * d_qk + d_v)
+    for l, (wq, wk, wv) in enumerate(layers):
+        for name, w, rows in (("Wq", wq, H * d_qk), ("Wk", wk, H * d_qk), ("Wv", wv, H * d_v)):
+            _need_cuda(w, f"layer {l} {name}", torch.bfloat16)
+            if tuple(w.shape) != (rows, D):
+                raise ValueError(f"layer {l} {name}: expected {(rows, D)}, got {tuple(w.shape)}")
+    if out is None:
+        W8 = torch.empty((L, N, D), dtype=torch.uint8, device=dev)
+        W8T = torch.empty((L, D, N), dtype=torch.uint8, device=dev)
+        w_scale = torch.empty((L,), dtype=torch.float32, device=dev)
+    else:
+        W8, W8T, w_scale = out
+    nws = int(lib().qkvp_bank_workspace_bytes(L, D, H, d_qk, d_v))
+    if nws == 0:
+        raise QKVPError(ERR_UNSUPPORTED, "qkvp_bank_workspace_bytes")
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    arr = lambda i: (ctypes.c_void_p * L)(*[ctypes.c_void_p(layers[l][i].data_ptr()) for l in range(L)])
+    _check(lib().qkvp_quantize_bank(L, D, H, d_qk, d_v, arr(0), arr(1), arr(2), _ptr(W8), _ptr(W8T),
+                                    _ptr(w_scale), _ptr(ws), nws, _stream(dev)), "qkvp_quantize_bank")
+    return W8, W8T, w_scale
+
+
+class QKVPBank:
+    """The FP8 weight bank of L layers, refreshed once per optimizer update.
+
+    ``refresh`` re-quantises when any weight tensor changed since the last
+    refresh (tracked by the tensors' version counters and storage pointers),
+    so the cached row-major and transposed views are never stale.
+    """
+
+    def __init__(self, layers, H: int, d_qk: int = 96, d_v: int = 128):
+        self.layers = [tuple(l) for l in layers]
+        self.H, self.d_qk, self.d_v = H, d_qk, d_v
+        self._key = None
+        self.W8 = self.W8T = self.w_scale = None
+        self.refreshes = 0
+        self.refresh()
+
+    def _state(self):
+        return tuple((w._version, w.data_ptr()) for l in self.layers for w in l)
+
+    def refresh(self, force: bool = False) -> bool:
+        key = self._state()
+        if not force and key == self._key:
+            return False
+        out = None if self.W8 is None else (self.W8, self.W8T, self.w_scale)
+        self.W8, self.W8T, self.w_scale = quantize_bank(self.layers, self.H, self.d_qk, self.d_v, out=out)
+        self._key = key
+        self.refreshes += 1
+        return True
+
+    def layer(self, l: int):
+        return self.W8[l], self.W8T[l], self.w_scale[l:l + 1]
+
+
+# ----------------------------------------------------------------------------
+# Forward / backward
+# ----------------------------------------------------------------------------
+
+@dataclass
+class Saved:
+    """State the backward needs: saved outputs and the FP8 activations."""
+    q: torch.Tensor
+    k: torch.Tensor
+    rstd: torch.Tensor
+    x8T: torch.Tensor
+    x_scale: torch.Tensor
+    pos: torch.Tensor
+
+
+def forward(x, pos, W8, w_scale, H, rope_table, d_qk=96, d_v=128, eps=1e-6, ws=None, out=None):
+    """Packed QKV forward for one layer.
+
+    x [T, D] bf16, pos [T] int32, W8 [N, D] uint8, w_scale [1] float32,
+    rope_table from build_rope_table.  Returns (q, k, v, Saved, x8) with
+    q, k [H, T, d_qk] and v [H, T, d_v] bf16.
+    """
+    T, D = x.shape
+    shape = Shape(T, D, H, d_qk, d_v)
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(pos, "pos", torch.int32)
+    _need_cuda(W8, "W8", torch.uint8)
+    _need_cuda(w_scale, "w_scale", torch.float32)
+    _need_cuda(rope_table, "rope_table", torch.float32)
+    dev = x.device
+    if ws is None:
+        ws = new_workspace(shape, dev)
+    if out is None:
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        out = dict(q=torch.empty((H, T, d_qk), **bf), k=torch.empty((H, T, d_qk), **bf),
+                   v=torch.empty((H, T, d_v), **bf),
+                   rstd=torch.empty((2, H, T), dtype=torch.float32, device=dev),
+                   x8=torch.empty((T, D), dtype=torch.uint8, device=dev),
+                   x8T=torch.empty((D, shape.Tp), dtype=torch.uint8, device=dev),
+                   x_scale=torch.empty((1,), dtype=torch.float32, device=dev))
+    o = out
+    d = shape.dims()
+    rc = lib().qkvp_forward(ctypes.byref(d), eps, _ptr(rope_table), rope_table.shape[1], _ptr(x), _ptr(pos),
+                            _ptr(W8), _ptr(w_scale), _ptr(o["q"]), _ptr(o["k"]), _ptr(o["v"]), _ptr(o["rstd"]),
+                            _ptr(o["x8"]), _ptr(o["x8T"]), _ptr(o["x_scale"]), _ptr(ws), ws.numel(),
+                            _stream(dev))
+    _check(rc, "qkvp_forward")
+    saved = Saved(q=o["q"], k=o["k"], rstd=o["rstd"], x8T=o["x8T"], x_scale=o["x_scale"], pos=pos)
+    return o["q"], o["k"], o["v"], saved, o["x8"]
+
+
+def backward(dq, dk, dv, saved: Saved, W8T, w_scale, rope_table, ws=None, out=None):
+    """Packed QKV backward for one layer.  Returns a dict with dx [T, D],
+    dW [N, D] (bf16), dY8 [T, N], dY8T [N, Tp] (uint8) and dy_scale [1]."""
+    H, T, d_qk = dq.shape
+    d_v = dv.shape[2]
+    D = W8T.shape[0]
+    shape = Shape(T, D, H, d_qk, d_v)
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need_cuda(t, name, torch.bfloat16)
+    _need_cuda(W8T, "W8T", torch.uint8)
+    dev = dq.device
+    if ws is None:
+        ws = new_workspace(shape, dev)
+    if out is None:
+        out = dict(dx=torch.empty((T, D), dtype=torch.bfloat16, device=dev),
+                   dW=torch.empty((shape.N, D), dtype=torch.bfloat16, device=dev),
+                   dY8=torch.empty((T, shape.N), dtype=torch.uint8, device=dev),
+                   dY8T=torch.empty((shape.N, shape.Tp), dtype=torch.uint8, device=dev),
+                   dy_scale=torch.empty((1,), dtype=torch.float32, device=dev))
+    o = out
+    d = shape.dims()
+    rc = lib().qkvp_backward(ctypes.byref(d), _ptr(rope_table), rope_table.shape[1], _ptr(dq), _ptr(dk), _ptr(dv),
+                             _ptr(saved.q), _ptr(saved.k), _ptr(saved.rstd), _ptr(saved.pos), _ptr(W8T),
+                             _ptr(w_scale), _ptr(saved.x8T), _ptr(saved.x_scale), _ptr(o["dx"]), _ptr(o["dW"]),
+                             _ptr(o["dY8"]), _ptr(o["dY8T"]), _ptr(o["dy_scale"]), _ptr(ws), ws.numel(),
+                             _stream(dev))
+    _check(rc, "qkvp_backward")
+    return o

@@ -74,7 +74,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // gives up after st.timeout_ns, or as soon as another role of the CTA has set
 // *abort.  On expiry records QKVP_ERR_TIMEOUT and sets *abort.  Returns true
 // when the phase completed.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                        const DevStatus& st, int kid) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();

@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.  Integer work (FP8 codes, layouts, scales) must be
+bit-exact; floating-point outputs must satisfy max|err| <= 2e-2 * rms(ref)
+and relative Frobenius error <= 5e-3."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import assert_close, assert_codes_match
+
+pytestmark = pytest.mark.gpu
+
+f32 = synth.to_numpy_f32
+
+
+@pytest.fixture(scope="module")
+def qk():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fp8_packed_reduced_gb300 import build as b
+    b.build()
+    import fp8_packed_reduced_gb300 as pkg
+    pkg.lib()
+    return pkg
+
+
+DEV = "cuda:0"
+
+
+def _bank(qk, inp, s):
+    layers = [tuple(inp[k].to(DEV) for k in ("Wq", "Wk", "Wv"))]
+    W8, W8T, w_scale = qk.quantize_bank(layers, s.H, s.d_qk, s.d_v)
+    oW8, oW8T, os_w = oracle.quantize_bank(*(f32(inp[k]) for k in ("Wq", "Wk", "Wv")))
+    return (W8[0], W8T[0], w_scale[0:1]), (oW8, oW8T, os_w)
+
+
+def _run_forward(qk, s, seed=0):
+    inp = synth.forward_inputs(s, seed=seed)
+    (W8, W8T, w_scale), (oW8, oW8T, os_w) = _bank(qk, inp, s)
+    table = qk.build_rope_table(s.seq_len, s.d_qk, 10000.0, DEV)
+    x, pos = inp["x"].to(DEV), inp["pos"].to(DEV)
+    ws = qk.new_workspace(qk.Shape(s.T, s.D, s.H, s.d_qk, s.d_v), DEV)
+    q, k, v, saved, x8 = qk.forward(x, pos, W8, w_scale, s.H, table, s.d_qk, s.d_v, ws=ws)
+    torch.cuda.synchronize()
+    return dict(inp=inp, W8=W8, W8T=W8T, w_scale=w_scale, oW8=oW8, os_w=os_w, table=table, ws=ws,
+                q=q, k=k, v=v, saved=saved, x8=x8)
+
+
+SHAPES = [
+    synth.TINY,                                                   # T=128, D=768, H=6, 96/96/128
+    synth.Shape(T=200, D=768, H=6, d_qk=96, d_v=128, seq_len=64),  # ragged token tail
+    synth.Shape(T=1, D=768, H=6, d_qk=96, d_v=128, seq_len=8),     # a single token
+    synth.Shape(T=300, D=1024, H=8, d_qk=64, d_v=128, seq_len=256),
+    synth.Shape(T=260, D=1024, H=8, d_qk=128, d_v=128, seq_len=256),
+    synth.Shape(T=384, D=2048, H=16, d_qk=96, d_v=128, seq_len=384),
+    synth.Shape(T=130, D=640, H=5, d_qk=96, d_v=128, seq_len=130),  # odd head count, D % 256 != 0
+]
+IDS = [f"T{s.T}_D{s.D}_H{s.H}_dqk{s.d_qk}" for s in SHAPES]
+
+
+# ----------------------------------------------------------------------------
+# Bank refresh
+# ----------------------------------------------------------------------------
+
+def test_bank_twelve_layers_bit_exact_and_refresh(qk):
+    H, D = 6, 768
+    layers = synth.bank_layers(12, H=H, D=D, seed=100)
+    dev_layers = [tuple(w.to(DEV) for w in l) for l in layers]
+    bank = qk.QKVPBank(dev_layers, H)
+    torch.cuda.synchronize()
+    for l in (0, 5, 11):
+        oW8, oW8T, os_w = oracle.quantize_bank(*(f32(w) for w in layers[l]))
+        np.testing.assert_array_equal(bank.W8[l].cpu().numpy(), oW8)
+        np.testing.assert_array_equal(bank.W8T[l].cpu().numpy(), oW8T)
+        assert bank.w_scale[l].item() == float(os_w)
+    np.testing.assert_array_equal(bank.W8T.cpu().numpy(), bank.W8.transpose(1, 2).cpu().numpy())
+    assert not bank.refresh()                       # nothing changed: cache kept
+    # optimizer update: nudge every tensor in place, the cache is refreshed
+    upd = synth.bank_layers(12, H=H, D=D, seed=100, perturb=1e-3)
+    for l in range(12):
+        for j in range(3):
+            dev_layers[l][j].copy_(upd[l][j].to(DEV))
+    assert bank.refresh() and bank.refreshes == 2
+    torch.cuda.synchronize()
+    for l in (0, 11):
+        oW8, oW8T, os_w = oracle.quantize_bank(*(f32(w) for w in upd[l]))
+        np.testing.assert_array_equal(bank.W8[l].cpu().numpy(), oW8)
+        np.testing.assert_array_equal(bank.W8T[l].cpu().numpy(), oW8T)
+        assert bank.w_scale[l].item() == float(os_w)
+
+
+@pytest.mark.parametrize("H,D,dqk", [(5, 640, 96), (8, 1024, 64), (3, 384, 128)])
+def test_bank_other_shapes(qk, H, D, dqk):
+    layers = synth.bank_layers(2, H=H, D=D, d_qk=dqk, seed=7)
+    W8, W8T, s = qk.quantize_bank([tuple(w.to(DEV) for w in l) for l in layers], H, dqk, 128)
+    for l in range(2):
+        oW8, oW8T, os_w = oracle.quantize_bank(*(f32(w) for w in layers[l]))
+        np.testing.assert_array_equal(W8[l].cpu().numpy(), oW8)
+        np.testing.assert_array_equal(W8T[l].cpu().numpy(), oW8T)
+        assert s[l].item() == float(os_w)
+
+
+# ----------------------------------------------------------------------------
+# Forward
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("s", SHAPES, ids=IDS)
+def test_forward_matches_oracle(qk, s):
+    r = _run_forward(qk, s)
+    inp = r["inp"]
+    fw = oracle.forward(f32(inp["x"]), r["oW8"], r["os_w"], inp["pos"].numpy(), s.H, s.d_qk, s.d_v)
+    assert r["saved"].x_scale.item() == float(fw["x_scale"])
+    np.testing.assert_array_equal(r["x8"].cpu().numpy(), fw["x8"])
+    x8T = r["saved"].x8T.cpu().numpy()
+    np.testing.assert_array_equal(x8T[:, :s.T], fw["x8"].T)
+    assert not x8T[:, s.T:].any(), "padding columns of x8T must hold zero codes"
+    for name in ("q", "k", "v"):
+        assert_close(f32(r[name]), fw[name], name)
+    assert_close(r["saved"].rstd.cpu().numpy(), fw["rstd"], "rstd")
+
+
+def test_forward_deterministic(qk):
+    s = synth.Shape(T=520, D=768, H=6, seq_len=512)
+    a, b = _run_forward(qk, s), _run_forward(qk, s)
+    for name in ("q", "k", "v", "x8"):
+        assert torch.equal(a[name], b[name]), name
+
+
+# ----------------------------------------------------------------------------
+# Backward
+# ----------------------------------------------------------------------------
+
+def _run_backward(qk, s, seed=0):
+    """Backward with the saved state taken from the oracle's forward (rounded
+    to the saved precisions), so that both sides start from the same point."""
+    r = _run_forward(qk, s, seed)
+    inp = r["inp"]
+    pos = inp["pos"].numpy()
+    fw = oracle.forward(f32(inp["x"]), r["oW8"], r["os_w"], pos, s.H, s.d_qk, s.d_v)
+    g = synth.backward_inputs(s, seed=seed)
+    q_saved = torch.tensor(fw["q"]).to(torch.bfloat16)
+    k_saved = torch.tensor(fw["k"]).to(torch.bfloat16)
+    rstd_saved = torch.tensor(fw["rstd"]).to(torch.float32)
+    saved = qk.Saved(q=q_saved.to(DEV), k=k_saved.to(DEV), rstd=rstd_saved.to(DEV),
+                     x8T=r["saved"].x8T, x_scale=r["saved"].x_scale, pos=inp["pos"].to(DEV))
+    out = qk.backward(*(g[n].to(DEV) for n in ("dq", "dk", "dv")), saved, r["W8T"], r["w_scale"], r["table"],
+                      ws=r["ws"])
+    torch.cuda.synchronize()
+    bw = oracle.backward(*(f32(g[n]) for n in ("dq", "dk", "dv")), f32(q_saved), f32(k_saved),
+                         rstd_saved.numpy(), pos, r["oW8"], r["os_w"], fw["x8"], fw["x_scale"],
+                         s.H, s.d_qk, s.d_v)
+    return out, bw, r, fw
+
+
+@pytest.mark.parametrize("s", SHAPES, ids=IDS)
+def test_backward_matches_oracle(qk, s):
+    out, bw, r, fw = _run_backward(qk, s)
+    dy_scale = out["dy_scale"].item()
+    assert abs(dy_scale - float(bw["dy_scale"])) <= 1e-6 * float(bw["dy_scale"])
+    dY8 = out["dY8"].cpu().numpy()
+    assert_codes_match(dY8, bw["dY8"], "dY8")
+    dY8T = out["dY8T"].cpu().numpy()
+    np.testing.assert_array_equal(dY8T[:, :s.T], dY8.T)
+    assert not dY8T[:, s.T:].any(), "padding columns of dY8T must hold zero codes"
+    assert_close(f32(out["dx"]), bw["dX"], "dx")
+    assert_close(f32(out["dW"]), bw["dW"], "dW")
+
+
+def test_gradient_gemms_on_the_same_codes(qk):
+    """dX and dW from the GPU's own dY8 codes: isolates the two GEMMs."""
+    s = synth.Shape(T=640, D=768, H=6, seq_len=640)
+    out, bw, r, fw = _run_backward(qk, s, seed=3)
+    dX, dW = oracle.grad_gemms(out["dY8"].cpu().numpy(), np.float32(out["dy_scale"].item()), r["oW8"], r["os_w"],
+                               fw["x8"], fw["x_scale"])
+    assert_close(f32(out["dx"]), dX, "dx (same codes)")
+    assert_close(f32(out["dW"]), dW, "dW (same codes)")
+
+
+def test_backward_deterministic(qk):
+    s = synth.Shape(T=1000, D=768, H=6, seq_len=1000)
+    a, _, _, _ = _run_backward(qk, s, seed=5)
+    b, _, _, _ = _run_backward(qk, s, seed=5)
+    for name in ("dx", "dW", "dY8", "dY8T"):
+        assert torch.equal(a[name], b[name]), name
+
+
+# ----------------------------------------------------------------------------
+# Device-side error reporting (no fault, no hang)
+# ----------------------------------------------------------------------------
+
+def test_wait_timeout_is_reported_and_context_survives(qk):
+    ws = qk.new_workspace(qk.Shape(128, 768, 6), DEV)
+    assert qk.poll_device_status(ws) == (qk.OK, 0)
+    qk.selftest_wait_timeout(ws, 2000)         # a barrier nothing arrives on, 2 ms limit
+    code, where = qk.poll_device_status(ws)
+    assert code == qk.ERR_TIMEOUT and where == 11
+    assert qk.poll_device_status(ws) == (qk.OK, 0)
+    # the context is still usable
+    r = _run_forward(qk, synth.TINY)
+    assert torch.isfinite(r["q"].float()).all()
+
+
+def test_position_outside_table_is_reported(qk):
+    s = synth.TINY
+    inp = synth.forward_inputs(s)
+    (W8, W8T, w_scale), _ = _bank(qk, inp, s)
+    table = qk.build_rope_table(64, s.d_qk, 10000.0, DEV)      # positions reach 127
+    ws = qk.new_workspace(qk.Shape(s.T, s.D, s.H), DEV)
+    qk.forward(inp["x"].to(DEV), inp["pos"].to(DEV), W8, w_scale, s.H, table, ws=ws)
+    code, where = qk.poll_device_status(ws)
+    assert code == qk.ERR_DEVICE_INPUT and where == 5

@@ -1,0 +1,397 @@
+#!/usr/bin/env python3
+"""Benchmark of the packed FP8 QKV projection, forward + backward, on GB300.
+
+One step = one pass of the whole hot path over one batch: the per-update bank
+refresh of the layer (amax + dual-layout quantisation), the forward (x amax,
+x quantisation, packed GEMM with the fused split/RMSNorm/RoPE epilogue) and
+the backward (dY amax, dY quantisation, dX GEMM, dW GEMM, dW reduction).
+Workload: 6 sequences x 8192 tokens (T = 49152), D = 768, H = 6, d_qk = 96,
+d_v = 128, synthetic seeded inputs.
+
+Prints one JSON line (rank 0).  `--impl reference` times the plain CPU oracle
+on the host cores instead, each step one bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "packed-QKV fwd+bwd tokens/s"
+KERNELS = ["bank_amax", "bank_quant", "x_amax", "x_quant", "fwd_gemm",
+           "dy_amax", "dy_quant", "dx_gemm", "dw_gemm", "dw_reduce"]
+# event index pairs bracketing each kernel (see qkvp_set_timing_events)
+SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (5, 6), (7, 8), (8, 9), (9, 10), (10, 11), (11, 12)]
+EVENTS_PER_STEP = 13
+
+
+def algorithmic_work(s: synth.Shape):
+    """Bytes (HBM-bound kernels) or FLOPs (GEMMs) one launch must move or do."""
+    T, D, H, dqk, dv, N = s.T, s.D, s.H, s.d_qk, s.d_v, s.N
+    bank = N * D * 2
+    q_bytes = H * T * dqk * 2
+    v_bytes = H * T * dv * 2
+    rstd = 2 * H * T * 4
+    bwd_in = 2 * q_bytes + v_bytes + 2 * q_bytes + rstd + T * 4
+    flops = 2.0 * T * D * N
+    return {
+        "bank_amax": ("hbm", bank),
+        "bank_quant": ("hbm", bank + 2 * N * D),
+        "x_amax": ("hbm", T * D * 2),
+        "x_quant": ("hbm", T * D * 2 + 2 * T * D),
+        "fwd_gemm": ("tensor", flops),
+        "dy_amax": ("hbm", bwd_in),
+        "dy_quant": ("hbm", bwd_in + 2 * T * N),
+        "dx_gemm": ("tensor", flops),
+        "dw_gemm": ("tensor", flops),
+        "dw_reduce": ("hbm", N * D * 2),
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p["bf16_tflops_sustained"]), source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
+                                 hw=f[4], hwt=f[5], swt=f[6], pcap=f[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [r for r in rows if r["power"] > 0] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["smax"] for r in busy),
+                "samples": len(busy), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# CUDA path
+# ----------------------------------------------------------------------------
+
+class Step:
+    """Inputs resident in HBM, preallocated outputs and workspace: one call of
+    step() runs the whole hot path once on the current stream."""
+
+    def __init__(self, s: synth.Shape, dev):
+        import fp8_packed_reduced_gb300 as qk
+        self.qk, self.s, self.dev = qk, s, dev
+        inp = synth.forward_inputs(s, seed=0, device=dev)
+        g = synth.backward_inputs(s, seed=0, device=dev)
+        self.layers = [(inp["Wq"], inp["Wk"], inp["Wv"])]
+        self.x, self.pos = inp["x"], inp["pos"]
+        self.dq, self.dk, self.dv = g["dq"], g["dk"], g["dv"]
+        self.table = qk.build_rope_table(s.seq_len, s.d_qk, 10000.0, dev)
+        shp = qk.Shape(s.T, s.D, s.H, s.d_qk, s.d_v)
+        self.ws = qk.new_workspace(shp, dev)
+        N, T, D, H = s.N, s.T, s.D, s.H
+        u8, bf = dict(dtype=torch.uint8, device=dev), dict(dtype=torch.bfloat16, device=dev)
+        self.bank = (torch.empty((1, N, D), **u8), torch.empty((1, D, N), **u8),
+                     torch.empty((1,), dtype=torch.float32, device=dev))
+        self.fwd_out = dict(q=torch.empty((H, T, s.d_qk), **bf), k=torch.empty((H, T, s.d_qk), **bf),
+                            v=torch.empty((H, T, s.d_v), **bf),
+                            rstd=torch.empty((2, H, T), dtype=torch.float32, device=dev),
+                            x8=torch.empty((T, D), **u8), x8T=torch.empty((D, shp.Tp), **u8),
+                            x_scale=torch.empty((1,), dtype=torch.float32, device=dev))
+        self.bwd_out = dict(dx=torch.empty((T, D), **bf), dW=torch.empty((N, D), **bf),
+                            dY8=torch.empty((T, N), **u8), dY8T=torch.empty((N, shp.Tp), **u8),
+                            dy_scale=torch.empty((1,), dtype=torch.float32, device=dev))
+
+    def step(self):
+        qk = self.qk
+        W8, W8T, ws_ = qk.quantize_bank(self.layers, self.s.H, self.s.d_qk, self.s.d_v, out=self.bank)
+        q, k, v, saved, _ = qk.forward(self.x, self.pos, W8[0], ws_[0:1], self.s.H, self.table, self.s.d_qk,
+                                       self.s.d_v, ws=self.ws, out=self.fwd_out)
+        qk.backward(self.dq, self.dk, self.dv, saved, W8T[0], ws_[0:1], self.table, ws=self.ws, out=self.bwd_out)
+
+
+def run_ours(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    from fp8_packed_reduced_gb300 import build as b
+    b.build()
+    import fp8_packed_reduced_gb300 as qk
+    s = synth.Shape(T=args.T, D=args.D, H=args.H, d_qk=args.dqk, d_v=128, seq_len=args.seq_len)
+    st = Step(s, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    code, where = qk.poll_device_status(st.ws)
+    if code != 0:
+        raise RuntimeError(f"device status {qk.STATUS.get(code)} from kernel {where}")
+
+    # per-kernel events for every timed step
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(EVENTS_PER_STEP)] for _ in range(args.steps)]
+    for ev in events:               # torch creates the CUDA event on its first record
+        for e in ev:
+            e.record(stream)
+    torch.cuda.synchronize()
+    assert all(e.cuda_event for ev in events for e in ev)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(max(3, args.warmup)):      # keep the GPU busy while the sampler starts
+        st.step()
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler.mark("t0")
+    t_start.record(stream)
+    for i in range(args.steps):
+        qk.set_timing_events(events[i])
+        st.step()
+    t_end.record(stream)
+    qk.set_timing_events([])
+    barrier()
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    clocks = sampler.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    code, where = qk.poll_device_status(st.ws)
+    if code != 0:
+        raise RuntimeError(f"device status {qk.STATUS.get(code)} from kernel {where}")
+
+    # per-kernel average durations (ms)
+    per = {k: 0.0 for k in KERNELS}
+    for ev in events:
+        for name, (a, b_) in zip(KERNELS, SPANS):
+            per[name] += ev[a].elapsed_time(ev[b_]) / args.steps
+    work = algorithmic_work(s)
+    peaks = load_peaks()
+    fp8_sus = 2.0 * peaks["bf16_sus"]       # E4M3 dense = 2 x bf16 dense (nominal ratio)
+    kern = {}
+    for name in KERNELS:
+        bound, amount = work[name]
+        t = per[name] * 1e-3
+        if bound == "hbm":
+            ach = amount / t / 1e9
+            kern[name] = dict(ms=round(per[name], 5), bound="hbm", achieved=round(ach, 1), unit="GB/s",
+                              frac=round(ach / peaks["hbm"], 4))
+        else:
+            ach = amount / t / 1e12
+            kern[name] = dict(ms=round(per[name], 5), bound="tensor", achieved=round(ach, 1), unit="TFLOP/s",
+                              frac=round(ach / fp8_sus, 4))
+    dom = max(KERNELS, key=lambda k: per[k])
+    bound, amount = work[dom]
+    roofline = dict(kernel=dom, bound=bound, achieved=kern[dom]["achieved"],
+                    peak=peaks["hbm"] if bound == "hbm" else round(fp8_sus, 1),
+                    unit=kern[dom]["unit"], frac=kern[dom]["frac"], traffic=None,
+                    peak_source=(f"{peaks['source']} HBM copy GB/s" if bound == "hbm" else
+                                 f"{peaks['source']} sustained bf16 x 2 (E4M3 nominal ratio)"),
+                    algorithmic=amount)
+
+    e2e = run_e2e(st, args, dev, world)
+    tokens = s.T * world
+    line = {
+        "metric": METRIC, "value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 GEMMs, fp32 accumulate, bf16 I/O",
+        "data": "synthetic (seeded N(0,1) activations and gradients, N(0,1/D) weights)",
+        "config": {"workload": f"packed QKV fwd+bwd, T={s.T} ({s.T // s.seq_len}x{s.seq_len}), D={s.D}, "
+                               f"H={s.H}, d_qk={s.d_qk}, d_v={s.d_v}, bank refresh per step",
+                   "T": s.T, "D": s.D, "H": s.H, "d_qk": s.d_qk, "d_v": s.d_v, "parallelism": f"replicas{world}",
+                   "l2": "no flush; one step touches ~1.3 GB, 10x the 129 MB L2"},
+        "roofline": roofline, "kernels": kern,
+        "gpu_launches": len(KERNELS) * args.steps,
+        "clocks": clocks, "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(s, args.cpu_sample)
+    return line
+
+
+def run_e2e(st: Step, args, dev, world):
+    """Same metric through the public API with pinned host buffers: every step
+    copies the step's inputs host->device and its results device->host."""
+    qk = st.qk
+    h = dict(x=st.x.cpu().pin_memory(), dq=st.dq.cpu().pin_memory(), dk=st.dk.cpu().pin_memory(),
+             dv=st.dv.cpu().pin_memory(), pos=st.pos.cpu().pin_memory())
+    res = dict(q=torch.empty_like(st.fwd_out["q"], device="cpu").pin_memory(),
+               k=torch.empty_like(st.fwd_out["k"], device="cpu").pin_memory(),
+               v=torch.empty_like(st.fwd_out["v"], device="cpu").pin_memory(),
+               dx=torch.empty_like(st.bwd_out["dx"], device="cpu").pin_memory(),
+               dW=torch.empty_like(st.bwd_out["dW"], device="cpu").pin_memory())
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in res.values())
+
+    def one():
+        st.x.copy_(h["x"], non_blocking=True)
+        st.pos.copy_(h["pos"], non_blocking=True)
+        st.dq.copy_(h["dq"], non_blocking=True)
+        st.dk.copy_(h["dk"], non_blocking=True)
+        st.dv.copy_(h["dv"], non_blocking=True)
+        st.step()
+        res["q"].copy_(st.fwd_out["q"], non_blocking=True)
+        res["k"].copy_(st.fwd_out["k"], non_blocking=True)
+        res["v"].copy_(st.fwd_out["v"], non_blocking=True)
+        res["dx"].copy_(st.bwd_out["dx"], non_blocking=True)
+        res["dW"].copy_(st.bwd_out["dW"], non_blocking=True)
+
+    steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        one()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(st.s.T * world / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (the reference arm and the cpu_baseline leg)
+# ----------------------------------------------------------------------------
+
+def oracle_step(s: synth.Shape, inp, g):
+    import oracle
+    f = synth.to_numpy_f32
+    W8, W8T, sw = oracle.quantize_bank(f(inp["Wq"]), f(inp["Wk"]), f(inp["Wv"]))
+    pos = inp["pos"].numpy()
+    fw = oracle.forward(f(inp["x"]), W8, sw, pos, s.H, s.d_qk, s.d_v)
+    oracle.backward(f(g["dq"]), f(g["dk"]), f(g["dv"]), fw["q"], fw["k"], fw["rstd"], pos, W8, sw, fw["x8"],
+                    fw["x_scale"], s.H, s.d_qk, s.d_v)
+
+
+def cpu_baseline(s: synth.Shape, sample_T: int):
+    sub = synth.Shape(T=sample_T, D=s.D, H=s.H, d_qk=s.d_qk, d_v=s.d_v, seq_len=s.seq_len)
+    inp, g = synth.forward_inputs(sub, 0), synth.backward_inputs(sub, 0)
+    t0 = time.perf_counter()
+    oracle_step(sub, inp, g)
+    dt = time.perf_counter() - t0
+    return {"value": round(sample_T / dt, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {sample_T} tokens of the workload (bank refresh + fwd + bwd), float64 NumPy, "
+                      f"{dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    s = synth.Shape(T=args.T, D=args.D, H=args.H, d_qk=args.dqk, d_v=128, seq_len=args.seq_len)
+    sub = synth.Shape(T=args.ref_sample, D=s.D, H=s.H, d_qk=s.d_qk, d_v=s.d_v, seq_len=s.seq_len)
+    inp, g = synth.forward_inputs(sub, 0), synth.backward_inputs(sub, 0)
+    for _ in range(args.warmup):
+        oracle_step(sub, inp, g)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sub, inp, g)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = round(sub.T / dt, 2)
+    sample = f"{sub.T} of the {s.T} tokens per step (bank refresh + fwd + bwd), float64 NumPy"
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (e4m3 codes emulated)", "data": "synthetic",
+        "config": {"workload": f"packed QKV fwd+bwd, T={s.T} ({s.T // s.seq_len}x{s.seq_len}), D={s.D}, "
+                               f"H={s.H}, d_qk={s.d_qk}, d_v={s.d_v}, bank refresh per step",
+                   "T": s.T, "D": s.D, "H": s.H, "d_qk": s.d_qk, "d_v": s.d_v},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--T", type=int, default=49152)
+    ap.add_argument("--D", type=int, default=768)
+    ap.add_argument("--H", type=int, default=6)
+    ap.add_argument("--dqk", type=int, default=96)
+    ap.add_argument("--seq-len", type=int, default=8192)
+    ap.add_argument("--cpu-sample", type=int, default=8192, help="tokens the oracle times for cpu_baseline")
+    ap.add_argument("--ref-sample", type=int, default=1024, help="tokens per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -69,10 +69,12 @@ def lib() -> ctypes.CDLL:
                                    + [ctypes.c_size_t, _P]),
             "qkvp_forward": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_float, _P, ctypes.c_int] + [_P] * 12
                              + [ctypes.c_size_t, _P]),
-            "qkvp_backward": (ctypes.c_int, [ctypes.POINTER(Dims), _P, ctypes.c_int] + [_P] * 18
+            "qkvp_backward": (ctypes.c_int, [ctypes.POINTER(Dims), _P, ctypes.c_int] + [_P] * 17
                               + [ctypes.c_size_t, _P]),
             "qkvp_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint, _P]),
             "qkvp_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
+            "qkvp_set_timing_events": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int]),
+            "qkvp_timing_events_recorded": (ctypes.c_int, []),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -151,6 +153,18 @@ def poll_device_status(ws: torch.Tensor):
     where = ctypes.c_int(0)
     code = lib().qkvp_poll_device_status(_ptr(ws), ctypes.byref(where), _stream(ws.device))
     return int(code), int(where.value)
+
+
+def set_timing_events(events):
+    """Arm the kernel-boundary timing hook with torch.cuda.Event objects
+    (created with enable_timing=True); an empty list disarms it."""
+    n = len(events)
+    arr = (ctypes.c_void_p * max(n, 1))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(lib().qkvp_set_timing_events(arr, n), "qkvp_set_timing_events")
+
+
+def timing_events_recorded() -> int:
+    return int(lib().qkvp_timing_events_recorded())
 
 
 def set_wait_timeout_ns(ns: int):

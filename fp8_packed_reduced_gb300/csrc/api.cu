@@ -131,6 +131,16 @@ int choose_splits(int tiles, int kblocks, int sms) {
 
 DevStatus dev_status(void* ws) { return DevStatus{static_cast<int*>(ws), g_timeout_ns}; }
 
+// Optional kernel-boundary events (qkvp_set_timing_events).
+struct TimingHook {
+  cudaEvent_t ev[256];
+  int n = 0, next = 0;
+} g_timing;
+
+void mark(cudaStream_t s) {
+  if (g_timing.next < g_timing.n) cudaEventRecord(g_timing.ev[g_timing.next++], s);
+}
+
 #define QKVP_TRY_CUDA(expr)                          \
   do {                                               \
     if ((expr) != cudaSuccess) return QKVP_ERR_CUDA; \
@@ -184,6 +194,16 @@ int qkvp_poll_device_status(void* ws, int* where, void* stream) {
   return host[0];
 }
 
+int qkvp_set_timing_events(void* const* events, int n) {
+  if (n < 0 || n > 256 || (n > 0 && !events)) return QKVP_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < n; ++i) g_timing.ev[i] = static_cast<cudaEvent_t>(events[i]);
+  g_timing.n = n;
+  g_timing.next = 0;
+  return QKVP_OK;
+}
+
+int qkvp_timing_events_recorded(void) { return g_timing.next; }
+
 int qkvp_set_wait_timeout_ns(uint64_t ns) {
   if (ns < 1000000ull || ns > 60000000000ull) return QKVP_ERR_INVALID_ARGUMENT;
   g_timeout_ns = ns;
@@ -234,7 +254,12 @@ int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v, const uint16_t* c
   a.Nq = H * d_qk;
   a.N = H * (2 * d_qk + d_v);
   float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
-  QKVP_TRY_CUDA(launch_bank_refresh(a, partials, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  mark(s);
+  QKVP_TRY_CUDA(launch_bank_amax(a, partials, s));
+  mark(s);
+  QKVP_TRY_CUDA(launch_bank_quant(a, partials, s));
+  mark(s);
   return QKVP_OK;
 }
 
@@ -273,8 +298,11 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   if (!ok) return QKVP_ERR_CUDA;
 
   const int nparts = std::min(kMaxParts, 4 * sms);
+  mark(s);
   QKVP_TRY_CUDA(launch_amax_bf16(x, static_cast<int64_t>(T) * D, xparts, nparts, s));
+  mark(s);
   QKVP_TRY_CUDA(launch_x_quant(tm_x, tm_x8, tm_x8t, static_cast<int>(Tp), D, xparts, nparts, x_scale, st, s));
+  mark(s);
 
   FwdParams p;
   p.T = T;
@@ -296,6 +324,7 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.rstd = rstd;
   const int grid = std::min(p.num_units, sms);
   QKVP_TRY_CUDA(launch_fwd_gemm(tm_x8, tm_w, tm_q, tm_k, tm_v, p, grid, st, s));
+  mark(s);
   return QKVP_OK;
 }
 
@@ -358,8 +387,11 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   bp.partials = dyparts;
   bp.nparts = std::min({bp.num_units, 3 * sms, kMaxParts});
   bp.dy_scale = dy_scale;
+  mark(s);
   QKVP_TRY_CUDA(launch_bwd_amax(m, bp, bp.nparts, st, s));
+  mark(s);
   QKVP_TRY_CUDA(launch_bwd_quant(m, bp, std::min(bp.num_units, 2 * sms), st, s));
+  mark(s);
 
   DxParams xp;
   xp.T = T;
@@ -371,6 +403,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   xp.dy_scale = dy_scale;
   xp.w_scale = w_scale;
   QKVP_TRY_CUDA(launch_dx_gemm(tm_dyA, tm_w8t, tm_dx, xp, std::min(xp.num_units, sms), st, s));
+  mark(s);
 
   const DwShape ds = dw_shape(dims);
   DwParams wp;
@@ -384,7 +417,9 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   wp.num_units = wp.splits * ds.m_tiles * ds.n_tiles;
   wp.partials = dwparts;
   QKVP_TRY_CUDA(launch_dw_gemm(tm_dytA, tm_x8tB, wp, std::min(wp.num_units, sms), st, s));
+  mark(s);
   QKVP_TRY_CUDA(launch_dw_reduce(wp, dy_scale, x_scale, dW, s));
+  mark(s);
   return QKVP_OK;
 }
 

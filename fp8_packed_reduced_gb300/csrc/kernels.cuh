@@ -22,7 +22,8 @@ struct BankArgs {
 };
 constexpr int kBankAmaxBlocks = 32;   // partial maxima per layer
 
-cudaError_t launch_bank_refresh(const BankArgs& a, float* partials, cudaStream_t s);
+cudaError_t launch_bank_amax(const BankArgs& a, float* partials, cudaStream_t s);
+cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Activation quantisation

@@ -132,10 +132,12 @@ __global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__
   }
 }
 
-cudaError_t launch_bank_refresh(const BankArgs& a, float* partials, cudaStream_t s) {
+cudaError_t launch_bank_amax(const BankArgs& a, float* partials, cudaStream_t s) {
   bank_amax_kernel<<<dim3(kBankAmaxBlocks, a.L), 256, 0, s>>>(a, partials);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStream_t s) {
   const int tiles = ((a.N + 127) / 128) * (a.D / 128);
   bank_quant_kernel<<<dim3(tiles, a.L), 256, 0, s>>>(a, partials);
   return cudaGetLastError();

@@ -183,6 +183,19 @@ int qkvp_selftest_wait_timeout(void* ws, size_t ws_bytes, unsigned timeout_us, v
 /* Device-side wait limit used by every kernel (default 2 s, 1 ms .. 60 s). */
 int qkvp_set_wait_timeout_ns(uint64_t ns);
 
+/* Kernel timing hook.  Arms `n` (<= 256) caller-created cudaEvent_t handles
+ * (HOST array, not copied beyond the handles themselves).  While armed, the
+ * calls above record the next unused event on their stream before their
+ * first kernel and after each kernel, so consecutive events bracket one
+ * kernel each.  Order of the kernels: qkvp_quantize_bank: amax, quantise;
+ * qkvp_forward: x amax, x quantise, forward GEMM; qkvp_backward: dY amax,
+ * dY quantise, dX GEMM, dW GEMM, dW reduction.  n = 0 disarms.  Not
+ * thread-safe; meant for benchmarks. */
+int qkvp_set_timing_events(void* const* events, int n);
+
+/* Number of events recorded since the last qkvp_set_timing_events. */
+int qkvp_timing_events_recorded(void);
+
 #ifdef __cplusplus
 }
 #endif

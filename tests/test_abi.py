@@ -65,10 +65,11 @@ def test_padded_tokens_and_workspace_sizes(qk):
 
 
 def _fwd(qk, dims, ws_bytes=1 << 40, eps=1e-6, max_pos=128, ptr=4096, null_at=None):
-    args = [ctypes.c_void_p(ptr) for _ in range(12)]
+    # args[0] is the rope table, args[1:] the 12 tensor pointers x .. ws, in order
+    args = [ctypes.c_void_p(ptr) for _ in range(13)]
     if null_at is not None:
         args[null_at] = None
-    return qk.lib().qkvp_forward(ctypes.byref(dims), eps, args[0], max_pos, *args[1:], args[-1], ws_bytes, None)
+    return qk.lib().qkvp_forward(ctypes.byref(dims), eps, args[0], max_pos, *args[1:], ws_bytes, None)
 
 
 def test_forward_validation_codes(qk):
@@ -86,8 +87,9 @@ def test_forward_validation_codes(qk):
 
 def test_backward_validation_codes(qk):
     good = qk.Dims(200, 1024, 8, 128, 128)
+    # P[0] is the rope table, P[1:] the 17 tensor pointers dq .. ws, in order
     P = [ctypes.c_void_p(8192) for _ in range(18)]
-    call = lambda dims, P, ws=1 << 40: qk.lib().qkvp_backward(ctypes.byref(dims), P[0], 64, *P[1:], P[0], ws, None)
+    call = lambda dims, P, ws=1 << 40: qk.lib().qkvp_backward(ctypes.byref(dims), P[0], 64, *P[1:], ws, None)
     assert call(qk.Dims(200, 1024, 8, 100, 128), P) == qk.ERR_UNSUPPORTED
     bad = list(P)
     bad[5] = None

@@ -96,13 +96,15 @@ def _stream(device: torch.device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def _need_cuda(t: torch.Tensor, name: str, dtype=None):
-    if not t.is_cuda:
+def _need_cuda(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+        raise ValueError(f"{name} must be contiguous (row-major)")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 # ----------------------------------------------------------------------------
@@ -276,10 +278,12 @@ def forward(x, pos, W8, w_scale, H, rope_table, d_qk=96, d_v=128, eps=1e-6, ws=N
     T, D = x.shape
     shape = Shape(T, D, H, d_qk, d_v)
     _need_cuda(x, "x", torch.bfloat16)
-    _need_cuda(pos, "pos", torch.int32)
-    _need_cuda(W8, "W8", torch.uint8)
-    _need_cuda(w_scale, "w_scale", torch.float32)
+    _need_cuda(pos, "pos", torch.int32, (T,))
+    _need_cuda(W8, "W8", torch.uint8, (shape.N, D))
+    _need_cuda(w_scale, "w_scale", torch.float32, (1,))
     _need_cuda(rope_table, "rope_table", torch.float32)
+    if rope_table.dim() != 3 or rope_table.shape[0] != d_qk // 2 or rope_table.shape[2] != 2:
+        raise ValueError("rope_table must be build_rope_table(max_pos, d_qk)")
     dev = x.device
     if ws is None:
         ws = new_workspace(shape, dev)
@@ -292,6 +296,11 @@ def forward(x, pos, W8, w_scale, H, rope_table, d_qk=96, d_v=128, eps=1e-6, ws=N
                    x8T=torch.empty((D, shape.Tp), dtype=torch.uint8, device=dev),
                    x_scale=torch.empty((1,), dtype=torch.float32, device=dev))
     o = out
+    for name, dt, shp in (("q", torch.bfloat16, (H, T, d_qk)), ("k", torch.bfloat16, (H, T, d_qk)),
+                          ("v", torch.bfloat16, (H, T, d_v)), ("rstd", torch.float32, (2, H, T)),
+                          ("x8", torch.uint8, (T, D)), ("x8T", torch.uint8, (D, shape.Tp)),
+                          ("x_scale", torch.float32, (1,))):
+        _need_cuda(o[name], name, dt, shp)
     d = shape.dims()
     rc = lib().qkvp_forward(ctypes.byref(d), eps, _ptr(rope_table), rope_table.shape[1], _ptr(x), _ptr(pos),
                             _ptr(W8), _ptr(w_scale), _ptr(o["q"]), _ptr(o["k"]), _ptr(o["v"]), _ptr(o["rstd"]),
@@ -309,9 +318,18 @@ def backward(dq, dk, dv, saved: Saved, W8T, w_scale, rope_table, ws=None, out=No
     d_v = dv.shape[2]
     D = W8T.shape[0]
     shape = Shape(T, D, H, d_qk, d_v)
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _need_cuda(t, name, torch.bfloat16)
-    _need_cuda(W8T, "W8T", torch.uint8)
+    _need_cuda(dq, "dq", torch.bfloat16)
+    _need_cuda(dk, "dk", torch.bfloat16, (H, T, d_qk))
+    _need_cuda(dv, "dv", torch.bfloat16, (H, T, d_v))
+    _need_cuda(saved.q, "saved q", torch.bfloat16, (H, T, d_qk))
+    _need_cuda(saved.k, "saved k", torch.bfloat16, (H, T, d_qk))
+    _need_cuda(saved.rstd, "saved rstd", torch.float32, (2, H, T))
+    _need_cuda(saved.pos, "pos", torch.int32, (T,))
+    _need_cuda(saved.x8T, "saved x8T", torch.uint8, (D, shape.Tp))
+    _need_cuda(saved.x_scale, "saved x_scale", torch.float32, (1,))
+    _need_cuda(W8T, "W8T", torch.uint8, (D, shape.N))
+    _need_cuda(w_scale, "w_scale", torch.float32, (1,))
+    _need_cuda(rope_table, "rope_table", torch.float32)
     dev = dq.device
     if ws is None:
         ws = new_workspace(shape, dev)
@@ -322,6 +340,10 @@ def backward(dq, dk, dv, saved: Saved, W8T, w_scale, rope_table, ws=None, out=No
                    dY8T=torch.empty((shape.N, shape.Tp), dtype=torch.uint8, device=dev),
                    dy_scale=torch.empty((1,), dtype=torch.float32, device=dev))
     o = out
+    for name, dt, shp in (("dx", torch.bfloat16, (T, D)), ("dW", torch.bfloat16, (shape.N, D)),
+                          ("dY8", torch.uint8, (T, shape.N)), ("dY8T", torch.uint8, (shape.N, shape.Tp)),
+                          ("dy_scale", torch.float32, (1,))):
+        _need_cuda(o[name], name, dt, shp)
     d = shape.dims()
     rc = lib().qkvp_backward(ctypes.byref(d), _ptr(rope_table), rope_table.shape[1], _ptr(dq), _ptr(dk), _ptr(dv),
                              _ptr(saved.q), _ptr(saved.k), _ptr(saved.rstd), _ptr(saved.pos), _ptr(W8T),

@@ -281,9 +281,10 @@ def forward(x, W8, s_w, pos, H, d_qk, d_v, eps=1e-6, base=10000.0,
     yq, rq = rms_norm(Yq, eps)
     yk, rk = rms_norm(Yk, eps)
     theta = rope_angles(np.asarray(pos)[idx], d_qk, base)
-    return dict(q=rope(yq, theta), k=rope(yk, theta), v=Yv,
-                rstd=np.stack([rq, rk]), x8=x8, x_scale=s_x, x_amax=amax,
-                y_q=yq, y_k=yk, Y=Y)
+    c = np.ascontiguousarray
+    return dict(q=c(rope(yq, theta)), k=c(rope(yk, theta)), v=c(Yv),
+                rstd=c(np.stack([rq, rk])), x8=x8, x_scale=s_x, x_amax=amax,
+                y_q=c(yq), y_k=c(yk), Y=Y)
 
 
 # ----------------------------------------------------------------------------

@@ -16,9 +16,18 @@ def err_stats(got, ref):
     return maxerr, rms, fro
 
 
-def assert_close(got, ref, name):
+def assert_close(got, ref, name, bf16_rounding=False):
+    """Both bounds.  With ``bf16_rounding`` the max bound also allows one bf16
+    rounding step of |ref| per element (2^-8 relative): used only where the
+    output is so heavy-tailed (a rank-one dW from a single token) that the
+    rounding of the largest element to the bf16 output alone exceeds
+    2e-2 * rms."""
     maxerr, rms, fro = err_stats(got, ref)
-    assert maxerr <= MAX_ERR_OVER_RMS * rms, f"{name}: max|err| {maxerr:.3e} > {MAX_ERR_OVER_RMS} * rms {rms:.3e}"
+    if bf16_rounding:
+        excess = np.abs(np.asarray(got, np.float64) - ref) - (MAX_ERR_OVER_RMS * rms + 2.0 ** -8 * np.abs(ref))
+        assert excess.max() <= 0, f"{name}: error beyond 2e-2*rms + one bf16 step"
+    else:
+        assert maxerr <= MAX_ERR_OVER_RMS * rms, f"{name}: max|err| {maxerr:.3e} > {MAX_ERR_OVER_RMS} * rms {rms:.3e}"
     assert fro <= REL_FROBENIUS, f"{name}: relative Frobenius error {fro:.3e} > {REL_FROBENIUS}"
 
 

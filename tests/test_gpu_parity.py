@@ -167,15 +167,16 @@ def test_backward_matches_oracle(qk, s):
     assert not dY8T[:, s.T:].any(), "padding columns of dY8T must hold zero codes"
     # The GEMMs judged on the GPU's own codes: identical inputs, unique result.
     dX, dW = oracle.grad_gemms(dY8, np.float32(dy_scale), r["oW8"], r["os_w"], fw["x8"], fw["x_scale"])
+    rank_one = s.T == 1      # dW is an outer product: see assert_close
     assert_close(f32(out["dx"]), dX, "dx (GPU codes)")
-    assert_close(f32(out["dW"]), dW, "dW (GPU codes)")
+    assert_close(f32(out["dW"]), dW, "dW (GPU codes)", bf16_rounding=rank_one)
     # The whole chain against the oracle's own codes.  Where a dY value sits
     # within float32 rounding of an E4M3 tie, both codes are correct results;
     # with one such code among few tokens a whole dW row moves by a grid step,
     # so this comparison is made when the codes agree everywhere.
     if np.array_equal(dY8, bw["dY8"]):
         assert_close(f32(out["dx"]), bw["dX"], "dx")
-        assert_close(f32(out["dW"]), bw["dW"], "dW")
+        assert_close(f32(out["dW"]), bw["dW"], "dW", bf16_rounding=rank_one)
 
 
 def test_gradient_gemms_on_the_same_codes(qk):

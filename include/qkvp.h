@@ -121,6 +121,27 @@ int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v,
                        uint8_t* W8, uint8_t* W8T, float* w_scale,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* Bank refresh that allocates nothing, for callers that cannot allocate
+ * device memory (no cudaMalloc of their own, no workspace to hand over: for
+ * example code confined to a framework's memory pool, or a refresh issued
+ * where an allocation could block).  The pages have no counterpart: this is a
+ * variant of qkvp_quantize_bank whose scratch (the per-layer partial maxima)
+ * lives in a fixed 16 KB array of device memory inside this library, held by
+ * every GPU that loads the library until the process exits.
+ *   Arguments and results: as qkvp_quantize_bank, without ws/ws_bytes.
+ *   L above 128 is rejected with QKVP_ERR_UNSUPPORTED (the array's capacity).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the one array, which keeps the previous call's
+ *   contents (nothing in it needs to start at zero).  Calls whose kernels
+ *   overlap on the GPU (different streams, or different host threads) race
+ *   on it: serialise them. */
+int qkvp_quantize_bank_static(int L, int D, int H, int d_qk, int d_v,
+                              const uint16_t* const* Wq, const uint16_t* const* Wk,
+                              const uint16_t* const* Wv,
+                              uint8_t* W8, uint8_t* W8T, float* w_scale, void* stream);
+
 /* Forward ("96 is enough", section "The change"): x is quantised with its own
  * scale, one FP8 GEMM x8 . W8^T (fp32 accumulate) gives the packed columns,
  * and its epilogue de-quantises, splits, RMS-normalises q and k per head

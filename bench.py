@@ -50,10 +50,10 @@ def algorithmic_work(s: synth.Shape):
         "bank_amax": ("hbm", bank),
         "bank_quant": ("hbm", bank + 2 * N * D),
         "x_amax": ("hbm", T * D * 2),
-        "x_quant": ("hbm", T * D * 2 + 2 * T * D),
+        "x_quant": ("hbm", T * D * 2 + T * D),
         "fwd_gemm": ("tensor", flops),
         "dy_amax": ("hbm", bwd_in),
-        "dy_quant": ("hbm", bwd_in + 2 * T * N),
+        "dy_quant": ("hbm", bwd_in + T * N),
         "dx_gemm": ("tensor", flops),
         "dw_gemm": ("tensor", flops),
         "dw_reduce": ("hbm", N * D * 2),
@@ -148,17 +148,17 @@ class Step:
         self.fwd_out = dict(q=torch.empty((H, T, s.d_qk), **bf), k=torch.empty((H, T, s.d_qk), **bf),
                             v=torch.empty((H, T, s.d_v), **bf),
                             rstd=torch.empty((2, H, T), dtype=torch.float32, device=dev),
-                            x8=torch.empty((T, D), **u8), x8T=torch.empty((D, shp.Tp), **u8),
+                            x8=torch.empty((T, D), **u8),
                             x_scale=torch.empty((1,), dtype=torch.float32, device=dev))
         self.bwd_out = dict(dx=torch.empty((T, D), **bf), dW=torch.empty((N, D), **bf),
-                            dY8=torch.empty((T, N), **u8), dY8T=torch.empty((N, shp.Tp), **u8),
+                            dY8=torch.empty((T, N), **u8),
                             dy_scale=torch.empty((1,), dtype=torch.float32, device=dev))
 
     def step(self):
         qk = self.qk
         W8, W8T, ws_ = qk.quantize_bank(self.layers, self.s.H, self.s.d_qk, self.s.d_v, out=self.bank)
-        q, k, v, saved, _ = qk.forward(self.x, self.pos, W8[0], ws_[0:1], self.s.H, self.table, self.s.d_qk,
-                                       self.s.d_v, ws=self.ws, out=self.fwd_out)
+        q, k, v, saved = qk.forward(self.x, self.pos, W8[0], ws_[0:1], self.s.H, self.table, self.s.d_qk,
+                                    self.s.d_v, ws=self.ws, out=self.fwd_out)
         qk.backward(self.dq, self.dk, self.dv, saved, W8T[0], ws_[0:1], self.table, ws=self.ws, out=self.bwd_out)
 
 

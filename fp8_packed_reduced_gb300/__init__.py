@@ -59,7 +59,6 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         sig = {
             "qkvp_status_string": (ctypes.c_char_p, [ctypes.c_int]),
-            "qkvp_padded_tokens": (ctypes.c_int64, [ctypes.c_int]),
             "qkvp_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Dims)]),
             "qkvp_bank_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 5),
             "qkvp_workspace_init": (ctypes.c_int, [_P, ctypes.c_size_t, _P]),
@@ -67,9 +66,9 @@ def lib() -> ctypes.CDLL:
             "qkvp_build_rope_table": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_double, _P]),
             "qkvp_quantize_bank": (ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.POINTER(_P)] * 3 + [_P] * 4
                                    + [ctypes.c_size_t, _P]),
-            "qkvp_forward": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_float, _P, ctypes.c_int] + [_P] * 12
+            "qkvp_forward": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_float, _P, ctypes.c_int] + [_P] * 11
                              + [ctypes.c_size_t, _P]),
-            "qkvp_backward": (ctypes.c_int, [ctypes.POINTER(Dims), _P, ctypes.c_int] + [_P] * 17
+            "qkvp_backward": (ctypes.c_int, [ctypes.POINTER(Dims), _P, ctypes.c_int] + [_P] * 16
                               + [ctypes.c_size_t, _P]),
             "qkvp_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint, _P]),
             "qkvp_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
@@ -123,16 +122,8 @@ class Shape:
     def N(self) -> int:
         return self.H * (2 * self.d_qk + self.d_v)
 
-    @property
-    def Tp(self) -> int:
-        return padded_tokens(self.T)
-
     def dims(self) -> Dims:
         return Dims(self.T, self.D, self.H, self.d_qk, self.d_v)
-
-
-def padded_tokens(T: int) -> int:
-    return int(lib().qkvp_padded_tokens(T))
 
 
 def workspace_bytes(shape: Shape) -> int:
@@ -263,7 +254,7 @@ class Saved:
     q: torch.Tensor
     k: torch.Tensor
     rstd: torch.Tensor
-    x8T: torch.Tensor
+    x8: torch.Tensor
     x_scale: torch.Tensor
     pos: torch.Tensor
 
@@ -272,8 +263,9 @@ def forward(x, pos, W8, w_scale, H, rope_table, d_qk=96, d_v=128, eps=1e-6, ws=N
     """Packed QKV forward for one layer.
 
     x [T, D] bf16, pos [T] int32, W8 [N, D] uint8, w_scale [1] float32,
-    rope_table from build_rope_table.  Returns (q, k, v, Saved, x8) with
-    q, k [H, T, d_qk] and v [H, T, d_v] bf16.
+    rope_table from build_rope_table.  Returns (q, k, v, Saved) with
+    q, k [H, T, d_qk] and v [H, T, d_v] bf16; Saved holds what the backward
+    needs (saved outputs, rstd, the FP8 activations x8 and their scale).
     """
     T, D = x.shape
     shape = Shape(T, D, H, d_qk, d_v)
@@ -293,27 +285,25 @@ def forward(x, pos, W8, w_scale, H, rope_table, d_qk=96, d_v=128, eps=1e-6, ws=N
                    v=torch.empty((H, T, d_v), **bf),
                    rstd=torch.empty((2, H, T), dtype=torch.float32, device=dev),
                    x8=torch.empty((T, D), dtype=torch.uint8, device=dev),
-                   x8T=torch.empty((D, shape.Tp), dtype=torch.uint8, device=dev),
                    x_scale=torch.empty((1,), dtype=torch.float32, device=dev))
     o = out
     for name, dt, shp in (("q", torch.bfloat16, (H, T, d_qk)), ("k", torch.bfloat16, (H, T, d_qk)),
                           ("v", torch.bfloat16, (H, T, d_v)), ("rstd", torch.float32, (2, H, T)),
-                          ("x8", torch.uint8, (T, D)), ("x8T", torch.uint8, (D, shape.Tp)),
-                          ("x_scale", torch.float32, (1,))):
+                          ("x8", torch.uint8, (T, D)), ("x_scale", torch.float32, (1,))):
         _need_cuda(o[name], name, dt, shp)
     d = shape.dims()
     rc = lib().qkvp_forward(ctypes.byref(d), eps, _ptr(rope_table), rope_table.shape[1], _ptr(x), _ptr(pos),
                             _ptr(W8), _ptr(w_scale), _ptr(o["q"]), _ptr(o["k"]), _ptr(o["v"]), _ptr(o["rstd"]),
-                            _ptr(o["x8"]), _ptr(o["x8T"]), _ptr(o["x_scale"]), _ptr(ws), ws.numel(),
+                            _ptr(o["x8"]), _ptr(o["x_scale"]), _ptr(ws), ws.numel(),
                             _stream(dev))
     _check(rc, "qkvp_forward")
-    saved = Saved(q=o["q"], k=o["k"], rstd=o["rstd"], x8T=o["x8T"], x_scale=o["x_scale"], pos=pos)
-    return o["q"], o["k"], o["v"], saved, o["x8"]
+    saved = Saved(q=o["q"], k=o["k"], rstd=o["rstd"], x8=o["x8"], x_scale=o["x_scale"], pos=pos)
+    return o["q"], o["k"], o["v"], saved
 
 
 def backward(dq, dk, dv, saved: Saved, W8T, w_scale, rope_table, ws=None, out=None):
     """Packed QKV backward for one layer.  Returns a dict with dx [T, D],
-    dW [N, D] (bf16), dY8 [T, N], dY8T [N, Tp] (uint8) and dy_scale [1]."""
+    dW [N, D] (bf16), dY8 [T, N] (uint8) and dy_scale [1]."""
     H, T, d_qk = dq.shape
     d_v = dv.shape[2]
     D = W8T.shape[0]
@@ -325,7 +315,7 @@ def backward(dq, dk, dv, saved: Saved, W8T, w_scale, rope_table, ws=None, out=No
     _need_cuda(saved.k, "saved k", torch.bfloat16, (H, T, d_qk))
     _need_cuda(saved.rstd, "saved rstd", torch.float32, (2, H, T))
     _need_cuda(saved.pos, "pos", torch.int32, (T,))
-    _need_cuda(saved.x8T, "saved x8T", torch.uint8, (D, shape.Tp))
+    _need_cuda(saved.x8, "saved x8", torch.uint8, (T, D))
     _need_cuda(saved.x_scale, "saved x_scale", torch.float32, (1,))
     _need_cuda(W8T, "W8T", torch.uint8, (D, shape.N))
     _need_cuda(w_scale, "w_scale", torch.float32, (1,))
@@ -337,18 +327,16 @@ def backward(dq, dk, dv, saved: Saved, W8T, w_scale, rope_table, ws=None, out=No
         out = dict(dx=torch.empty((T, D), dtype=torch.bfloat16, device=dev),
                    dW=torch.empty((shape.N, D), dtype=torch.bfloat16, device=dev),
                    dY8=torch.empty((T, shape.N), dtype=torch.uint8, device=dev),
-                   dY8T=torch.empty((shape.N, shape.Tp), dtype=torch.uint8, device=dev),
                    dy_scale=torch.empty((1,), dtype=torch.float32, device=dev))
     o = out
     for name, dt, shp in (("dx", torch.bfloat16, (T, D)), ("dW", torch.bfloat16, (shape.N, D)),
-                          ("dY8", torch.uint8, (T, shape.N)), ("dY8T", torch.uint8, (shape.N, shape.Tp)),
-                          ("dy_scale", torch.float32, (1,))):
+                          ("dY8", torch.uint8, (T, shape.N)), ("dy_scale", torch.float32, (1,))):
         _need_cuda(o[name], name, dt, shp)
     d = shape.dims()
     rc = lib().qkvp_backward(ctypes.byref(d), _ptr(rope_table), rope_table.shape[1], _ptr(dq), _ptr(dk), _ptr(dv),
                              _ptr(saved.q), _ptr(saved.k), _ptr(saved.rstd), _ptr(saved.pos), _ptr(W8T),
-                             _ptr(w_scale), _ptr(saved.x8T), _ptr(saved.x_scale), _ptr(o["dx"]), _ptr(o["dW"]),
-                             _ptr(o["dY8"]), _ptr(o["dY8T"]), _ptr(o["dy_scale"]), _ptr(ws), ws.numel(),
+                             _ptr(w_scale), _ptr(saved.x8), _ptr(saved.x_scale), _ptr(o["dx"]), _ptr(o["dW"]),
+                             _ptr(o["dY8"]), _ptr(o["dy_scale"]), _ptr(ws), ws.numel(),
                              _stream(dev))
     _check(rc, "qkvp_backward")
     return o

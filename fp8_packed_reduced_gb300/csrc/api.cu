@@ -72,8 +72,6 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int64_t padded_tokens(int T) { return (static_cast<int64_t>(T) + 127) / 128 * 128; }
-
 int check_dims(const qkvp_dims* d) {
   if (!d) return QKVP_ERR_INVALID_ARGUMENT;
   if (d->T < 1 || d->D < 1 || d->H < 1 || d->d_qk < 1 || d->d_v < 1) return QKVP_ERR_INVALID_ARGUMENT;
@@ -100,7 +98,7 @@ DwShape dw_shape(const qkvp_dims* d) {
   s.bn = d->D % 256 == 0 ? 256 : 128;
   s.m_tiles = (N + 127) / 128;
   s.n_tiles = d->D / s.bn;
-  s.kblocks_total = static_cast<int>(padded_tokens(d->T) / 128);
+  s.kblocks_total = (d->T + 127) / 128;
   return s;
 }
 size_t dw_partial_bytes(const DwShape& s, int splits) {
@@ -163,8 +161,6 @@ const char* qkvp_status_string(int status) {
     default: return "QKVP_ERR_UNKNOWN";
   }
 }
-
-int64_t qkvp_padded_tokens(int T) { return T < 1 ? -1 : padded_tokens(T); }
 
 size_t qkvp_workspace_bytes(const qkvp_dims* dims) {
   if (check_dims(dims) != QKVP_OK) return 0;
@@ -265,14 +261,13 @@ int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v, const uint16_t* c
 
 int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int max_pos, const uint16_t* x,
                  const int32_t* pos, const uint8_t* W8, const float* w_scale, uint16_t* q, uint16_t* k,
-                 uint16_t* v, float* rstd, uint8_t* x8, uint8_t* x8T, float* x_scale, void* ws, size_t ws_bytes,
-                 void* stream) {
+                 uint16_t* v, float* rstd, uint8_t* x8, float* x_scale, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_dims(dims);
   if (rc != QKVP_OK) return rc;
-  if (!rope_table || !x || !pos || !W8 || !w_scale || !q || !k || !v || !rstd || !x8 || !x8T || !x_scale || !ws)
+  if (!rope_table || !x || !pos || !W8 || !w_scale || !q || !k || !v || !rstd || !x8 || !x_scale || !ws)
     return QKVP_ERR_INVALID_ARGUMENT;
   if (max_pos < 1 || !(eps >= 0.f) || !(eps < 1.f)) return QKVP_ERR_INVALID_ARGUMENT;
-  const void* ptrs[] = {rope_table, x, pos, W8, w_scale, q, k, v, rstd, x8, x8T, x_scale, ws};
+  const void* ptrs[] = {rope_table, x, pos, W8, w_scale, q, k, v, rstd, x8, x_scale, ws};
   for (const void* p : ptrs)
     if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
   if (ws_bytes < ws_bytes_for(dims)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
@@ -281,16 +276,14 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
 
   const int T = dims->T, D = dims->D, H = dims->H, dqk = dims->d_qk, dv = dims->d_v;
   const int N = H * (2 * dqk + dv);
-  const int64_t Tp = padded_tokens(T);
+  const int tiles = (T + 127) / 128;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* xparts = reinterpret_cast<float*>(wsb + kStatusBytes);
   const DevStatus st = dev_status(ws);
 
-  CUtensorMap tm_x, tm_x8, tm_x8t, tm_w, tm_q, tm_k, tm_v;
-  bool ok = map2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, D, T, D * 2ull, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_x8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8T, Tp, D, Tp, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  CUtensorMap tm_x8, tm_w, tm_q, tm_k, tm_v;
+  bool ok = map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map3d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -298,10 +291,11 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   if (!ok) return QKVP_ERR_CUDA;
 
   const int nparts = std::min(kMaxParts, 4 * sms);
+  const int64_t n = static_cast<int64_t>(T) * D;
   mark(s);
-  QKVP_TRY_CUDA(launch_amax_bf16(x, static_cast<int64_t>(T) * D, xparts, nparts, s));
+  QKVP_TRY_CUDA(launch_amax_bf16(x, n, xparts, nparts, s));
   mark(s);
-  QKVP_TRY_CUDA(launch_x_quant(tm_x, tm_x8, tm_x8t, static_cast<int>(Tp), D, xparts, nparts, x_scale, st, s));
+  QKVP_TRY_CUDA(launch_x_quant(x, n, x8, xparts, nparts, x_scale, 4 * sms, s));
   mark(s);
 
   FwdParams p;
@@ -313,7 +307,7 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.nq = (H + p.hq - 1) / p.hq;
   p.nv = (H + 1) / 2;
   p.n_tiles = 2 * p.nq + p.nv;
-  p.num_units = static_cast<int>(Tp / 128) * p.n_tiles;
+  p.num_units = tiles * p.n_tiles;
   p.kblocks = D / 128;
   p.eps = eps;
   p.x_scale = x_scale;
@@ -330,16 +324,16 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
 
 int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, const uint16_t* dq,
                   const uint16_t* dk, const uint16_t* dv, const uint16_t* q, const uint16_t* k, const float* rstd,
-                  const int32_t* pos, const uint8_t* W8T, const float* w_scale, const uint8_t* x8T,
-                  const float* x_scale, uint16_t* dx, uint16_t* dW, uint8_t* dY8, uint8_t* dY8T, float* dy_scale,
-                  void* ws, size_t ws_bytes, void* stream) {
+                  const int32_t* pos, const uint8_t* W8T, const float* w_scale, const uint8_t* x8,
+                  const float* x_scale, uint16_t* dx, uint16_t* dW, uint8_t* dY8, float* dy_scale, void* ws,
+                  size_t ws_bytes, void* stream) {
   int rc = check_dims(dims);
   if (rc != QKVP_OK) return rc;
-  if (!rope_table || !dq || !dk || !dv || !q || !k || !rstd || !pos || !W8T || !w_scale || !x8T || !x_scale || !dx ||
-      !dW || !dY8 || !dY8T || !dy_scale || !ws)
+  if (!rope_table || !dq || !dk || !dv || !q || !k || !rstd || !pos || !W8T || !w_scale || !x8 || !x_scale || !dx ||
+      !dW || !dY8 || !dy_scale || !ws)
     return QKVP_ERR_INVALID_ARGUMENT;
   if (max_pos < 1) return QKVP_ERR_INVALID_ARGUMENT;
-  const void* ptrs[] = {rope_table, dq, dk, dv, q, k, rstd, pos, W8T, w_scale, x8T, x_scale, dx, dW, dY8, dY8T,
+  const void* ptrs[] = {rope_table, dq, dk, dv, q, k, rstd, pos, W8T, w_scale, x8, x_scale, dx, dW, dY8,
                         dy_scale, ws};
   for (const void* p : ptrs)
     if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
@@ -349,7 +343,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
 
   const int T = dims->T, D = dims->D, H = dims->H, dqk = dims->d_qk, dvw = dims->d_v;
   const int N = H * (2 * dqk + dvw);
-  const int64_t Tp = padded_tokens(T);
+  const int tiles = (T + 127) / 128;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* dyparts = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
@@ -363,13 +357,12 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   ok = ok && map3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&m.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, dvw, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map2d(&m.dy8, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-  ok = ok && map2d(&m.dy8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8T, Tp, N, Tp, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-  CUtensorMap tm_dyA, tm_w8t, tm_dx, tm_dytA, tm_x8tB;
-  ok = ok && map2d(&tm_dyA, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  // dY8 [T, N] read as 128 x 128 tiles: K-major A of the dX GEMM, MN-major A of the dW GEMM
+  CUtensorMap tm_dy, tm_w8t, tm_dx, tm_x8;
+  ok = ok && map2d(&tm_dy, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map2d(&tm_w8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8T, N, D, N, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dx, D, T, D * 2ull, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map2d(&tm_dytA, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8T, Tp, N, Tp, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_x8tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8T, Tp, D, Tp, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return QKVP_ERR_CUDA;
 
   BwdParams bp;
@@ -378,19 +371,19 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   bp.d_qk = dqk;
   bp.d_v = dvw;
   bp.N = N;
-  bp.tiles = static_cast<int>(Tp / 128);
-  bp.num_units = bp.tiles * H * 3;
+  bp.tiles = tiles;
+  bp.num_units = tiles * H * 3;
   bp.rstd = rstd;
   bp.pos = pos;
   bp.rope = rope_table;
   bp.max_pos = max_pos;
   bp.partials = dyparts;
-  bp.nparts = std::min({bp.num_units, 3 * sms, kMaxParts});
+  bp.nparts = std::min({bp.num_units, sms, kMaxParts});
   bp.dy_scale = dy_scale;
   mark(s);
   QKVP_TRY_CUDA(launch_bwd_amax(m, bp, bp.nparts, st, s));
   mark(s);
-  QKVP_TRY_CUDA(launch_bwd_quant(m, bp, std::min(bp.num_units, 2 * sms), st, s));
+  QKVP_TRY_CUDA(launch_bwd_quant(m, bp, std::min(bp.num_units, sms), st, s));
   mark(s);
 
   DxParams xp;
@@ -398,11 +391,11 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   xp.D = D;
   xp.bn = D % 256 == 0 ? 256 : 128;
   xp.n_tiles = D / xp.bn;
-  xp.num_units = bp.tiles * xp.n_tiles;
+  xp.num_units = tiles * xp.n_tiles;
   xp.kblocks = (N + 127) / 128;
   xp.dy_scale = dy_scale;
   xp.w_scale = w_scale;
-  QKVP_TRY_CUDA(launch_dx_gemm(tm_dyA, tm_w8t, tm_dx, xp, std::min(xp.num_units, sms), st, s));
+  QKVP_TRY_CUDA(launch_dx_gemm(tm_dy, tm_w8t, tm_dx, xp, std::min(xp.num_units, sms), st, s));
   mark(s);
 
   const DwShape ds = dw_shape(dims);
@@ -416,7 +409,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   wp.splits = choose_splits(ds.m_tiles * ds.n_tiles, ds.kblocks_total, sms);
   wp.num_units = wp.splits * ds.m_tiles * ds.n_tiles;
   wp.partials = dwparts;
-  QKVP_TRY_CUDA(launch_dw_gemm(tm_dytA, tm_x8tB, wp, std::min(wp.num_units, sms), st, s));
+  QKVP_TRY_CUDA(launch_dw_gemm(tm_dy, tm_x8, wp, std::min(wp.num_units, sms), st, s));
   mark(s);
   QKVP_TRY_CUDA(launch_dw_reduce(wp, dy_scale, x_scale, dW, s));
   mark(s);

@@ -184,6 +184,31 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Shared-memory matrix descriptor for an operand laid out by TMA with
+// 128-byte swizzling, general form: [0,14) start address >> 4, [16,30)
+// leading byte offset >> 4, [32,46) stride byte offset >> 4, [46,48) version
+// 1, [61,64) layout 2 (128-byte swizzle).
+//   K-major: rows of 128 bytes of K, 8-row atoms stacked along M/N every
+//            `sbo` bytes; the leading offset is unused.
+//   MN-major: 128 consecutive M/N elements per 128-byte row, rows along K;
+//            8-row atoms stacked along K every `sbo` bytes, 128-element
+//            column blocks along M/N every `lbo` bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor as above with A and/or B read MN-major (bit 15 for
+// A, bit 16 for B; allowed for 8-bit operands).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32_major(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_e4m3_f32(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
+}
+
 // Shared-memory matrix descriptor for a K-major operand laid out by TMA with
 // 128-byte swizzling: rows of 128 bytes, 8-row (1024 B) swizzle atoms stacked
 // along M/N.  Fields: [0,14) start address >> 4, [16,30) leading byte offset
@@ -225,6 +250,26 @@ __device__ __forceinline__ uint32_t quant1(float v, float s) {
 // Four codes packed little-endian (a in the lowest byte).
 __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float s) {
   return quant1(a, s) | (quant1(b, s) << 8) | (quant1(c, s) << 16) | (quant1(d, s) << 24);
+}
+
+// The same code as quant1(v, s), from a multiplication by rs = 1/s (rounded
+// to nearest).  q = v * rs is within 2^-22 (relative) of the IEEE quotient
+// fl(v/s), so the quotient lies inside [q (1 - 2^-20), q (1 + 2^-20)] (the
+// bracket's own rounding is 2^-24).  Rounding onto the E4M3 grid with
+// saturation is monotone, so when both ends of the bracket give the same code
+// that is the quotient's code; otherwise (q within 2^-20 of a rounding
+// boundary) the exact division decides.  For |q| below 2^-11 both ends and
+// the quotient give a signed zero of q's sign.
+__device__ __forceinline__ uint32_t quant1_fast(float v, float s, float rs) {
+  const float q = v * rs;
+  const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
+      make_float2(q * 0.99999904632568359375f, q * 1.00000095367431640625f), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t lo = c & 0xFFu, hi = (c >> 8) & 0xFFu;
+  return lo == hi ? lo : quant1(v, s);
+}
+__device__ __forceinline__ uint32_t quant4_fast(float a, float b, float c, float d, float s, float rs) {
+  return quant1_fast(a, s, rs) | (quant1_fast(b, s, rs) << 8) | (quant1_fast(c, s, rs) << 16) |
+         (quant1_fast(d, s, rs) << 24);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

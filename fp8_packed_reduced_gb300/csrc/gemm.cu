@@ -3,8 +3,9 @@
 //   forward  acc = x8 . W8^T        epilogue: de-quantise, split, per-head
 //                                   RMSNorm of q/k, RoPE, head-major bf16 store
 //   dX       acc = dY8 . W8         via W8T (K-major); epilogue: scale, bf16
-//   dW       acc = dY8^T . x8       via dY8T and x8T, split over K (tokens);
-//                                   fp32 partials, reduced in a fixed order
+//   dW       acc = dY8^T . x8       MN-major operands straight from dY8 and x8,
+//                                   split over K (tokens); fp32 partials,
+//                                   reduced in a fixed order
 //
 // One persistent, warp-specialised kernel body serves all three:
 //   warp 0     TMA producer: A tile (128 rows x 128 B of K) and B tile
@@ -62,9 +63,7 @@ __device__ void producer_role(const Sched& sc, const CUtensorMap* tmA, const CUt
     for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
       if (!mbar_wait(&g.empty[stage], phase ^ 1, &g.abort_flag, st, kid)) goto drain;
       mbar_arrive_expect_tx(&g.full[stage], static_cast<uint32_t>(kAStage + ui.ncols * kBK));
-      tma_load_2d(sA + stage * kAStage, tmA, &g.full[stage], kb * kBK, ui.a_row);
-      for (int j = 0; j < ui.ncols / 32; ++j)
-        tma_load_2d(sB + stage * kBStage + j * 32 * kBK, tmB, &g.full[stage], kb * kBK, ui.b_row + 32 * j);
+      sc.load(ui, kb, tmA, tmB, sA + stage * kAStage, sB + stage * kBStage, &g.full[stage]);
       used |= 1u << stage;
       last_par = (last_par & ~(1u << stage)) | (phase << stage);
       if (++stage == stages) {
@@ -92,7 +91,7 @@ __device__ void mma_role(const Sched& sc, uint8_t* sA, uint8_t* sB, GemmSmem& g,
     if (!mbar_wait(&g.tempty[buf], use ^ 1, &g.abort_flag, st, kid)) break;
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + buf * 256;
-    const uint32_t idesc = idesc_e4m3_f32(kBM, ui.ncols);
+    const uint32_t idesc = idesc_e4m3_f32_major(kBM, ui.ncols, Sched::kMN, Sched::kMN);
     bool ok = true;
     for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
       if (!mbar_wait(&g.full[stage], phase, &g.abort_flag, st, kid)) {
@@ -102,9 +101,13 @@ __device__ void mma_role(const Sched& sc, uint8_t* sA, uint8_t* sB, GemmSmem& g,
       tc_fence_after();
       const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBStage);
 #pragma unroll
-      for (int kk = 0; kk < kBK / 32; ++kk)
-        umma_e4m3(d_tmem, sdesc_k_sw128(a0 + kk * 32), sdesc_k_sw128(b0 + kk * 32), idesc,
-                  (kb > ui.kb0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < kBK / 32; ++kk) {
+        // K = 32 per instruction: 32 bytes along a K-major row, or 32 rows
+        // (four 8-row atoms) of an MN-major tile
+        const uint64_t ad = Sched::kMN ? sdesc_sw128(a0 + kk * 4096, 16384, 1024) : sdesc_k_sw128(a0 + kk * 32);
+        const uint64_t bd = Sched::kMN ? sdesc_sw128(b0 + kk * 4096, 16384, 1024) : sdesc_k_sw128(b0 + kk * 32);
+        umma_e4m3(d_tmem, ad, bd, idesc, (kb > ui.kb0 || kk > 0) ? 1u : 0u);
+      }
       umma_commit(&g.empty[stage]);
       if (++stage == stages) {
         stage = 0;
@@ -196,11 +199,24 @@ __device__ __forceinline__ void stage16(uint8_t* boxes, int row, int c0, const u
   stage_chunk_sw64(box, row, (c0 & 31) + 8, make_uint4(w[4], w[5], w[6], w[7]));
 }
 
+// K-major operands: A is one box of 128 rows x 128 bytes of K at (k, a_row);
+// B is ncols/32 boxes of 32 rows x 128 bytes at (k, b_row + 32 j).
+__device__ __forceinline__ void load_k_major(const Unit& ui, int kb, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                             uint8_t* sA, uint8_t* sB, uint64_t* bar) {
+  tma_load_2d(sA, tmA, bar, kb * kBK, ui.a_row);
+  for (int j = 0; j < ui.ncols / 32; ++j) tma_load_2d(sB + j * 32 * kBK, tmB, bar, kb * kBK, ui.b_row + 32 * j);
+}
+
 // ---------------------------------------------------------------------------
 // Forward: schedule and epilogue
 // ---------------------------------------------------------------------------
 struct FwdSched {
+  static constexpr bool kMN = false;
   const FwdParams& p;
+  __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
+                       uint8_t* sB, uint64_t* bar) const {
+    load_k_major(ui, kb, a, b, sA, sB, bar);
+  }
   __device__ int num_units() const { return p.num_units; }
   // kind 0 = q, 1 = k, 2 = v
   __device__ void decode(int j, int& kind, int& head0, int& nh) const {
@@ -374,7 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // dX: schedule and epilogue
 // ---------------------------------------------------------------------------
 struct DxSched {
+  static constexpr bool kMN = false;
   const DxParams& p;
+  __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
+                       uint8_t* sB, uint64_t* bar) const {
+    load_k_major(ui, kb, a, b, sA, sB, bar);
+  }
   __device__ int num_units() const { return p.num_units; }
   __device__ Unit unit(int u) const {
     Unit r;
@@ -444,10 +465,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dW: split-K schedule, fp32 partial epilogue, fixed-order reduction
+// dW: split-K schedule, fp32 partial epilogue, fixed-order reduction.
+// dW = dY8^T . x8 reads both operands MN-major straight from the token-major
+// tensors: a 128-token slice of dY8 [T, N] is the A tile (M = packed rows,
+// contiguous) and of x8 [T, D] the B tile (N = model columns, contiguous).
+// Token rows past T are zero-filled by TMA.
 // ---------------------------------------------------------------------------
 struct DwSched {
+  static constexpr bool kMN = true;
   const DwParams& p;
+  // A: one box of 128 tokens x 128 packed columns at (a_row, k); B: ncols/128
+  // boxes of 128 tokens x 128 model columns at (b_row + 128 j, k).
+  __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
+                       uint8_t* sB, uint64_t* bar) const {
+    tma_load_2d(sA, a, bar, ui.a_row, kb * kBK);
+    for (int j = 0; j < ui.ncols / 128; ++j) tma_load_2d(sB + j * 16384, b, bar, ui.b_row + 128 * j, kb * kBK);
+  }
   __device__ int num_units() const { return p.num_units; }
   __device__ Unit unit(int u) const {
     const int mn = p.m_tiles * p.n_tiles;

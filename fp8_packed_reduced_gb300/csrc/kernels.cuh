@@ -30,10 +30,9 @@ cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStre
 // ---------------------------------------------------------------------------
 // amax of n bf16 values at x (16-byte aligned); writes `blocks` partials.
 cudaError_t launch_amax_bf16(const uint16_t* x, int64_t n, float* partials, int blocks, cudaStream_t s);
-// x [T, D] -> x8 [T, D], x8T [D, Tp], x_scale; reads `nparts` partials.
-cudaError_t launch_x_quant(const CUtensorMap& tm_x, const CUtensorMap& tm_x8, const CUtensorMap& tm_x8t, int Tp,
-                           int D, const float* partials, int nparts, float* x_scale, DevStatus st,
-                           cudaStream_t s);
+// x (n bf16, n % 16 == 0) -> x8 codes and x_scale; reads `nparts` partials.
+cudaError_t launch_x_quant(const uint16_t* x, int64_t n, uint8_t* x8, const float* partials, int nparts,
+                           float* x_scale, int blocks, cudaStream_t s);
 
 cudaError_t launch_rope_table(float* table, int max_pos, int d_qk, double base, cudaStream_t s);
 cudaError_t launch_selftest_wait(DevStatus st, cudaStream_t s);
@@ -65,7 +64,7 @@ struct DxParams {
 };
 
 struct DwParams {
-  int N, D, bn, m_tiles, n_tiles, splits, num_units, kblocks_total;
+  int N, D, bn, m_tiles, n_tiles, splits, num_units, kblocks_total;   // kblocks_total = ceil(T/128)
   float* partials;    // [splits][m_tiles][n_tiles][bn][128] float32
 };
 
@@ -94,7 +93,7 @@ struct BwdParams {
 };
 struct BwdMaps {
   CUtensorMap dq, q, dk, k, dv;   // loads, 3-D [H][T][d], box {32, 128, 1}, 64-byte swizzle
-  CUtensorMap dy8, dy8t;          // stores: [T][N] box {32, 128}; [N][Tp] box {128, 32} 128-byte swizzle
+  CUtensorMap dy8;                // store: [T][N] codes, box {32, 128}
 };
 cudaError_t launch_bwd_amax(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s);
 cudaError_t launch_bwd_quant(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s);

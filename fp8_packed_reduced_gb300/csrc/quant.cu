@@ -1,7 +1,7 @@
 // Bandwidth-bound quantisation kernels:
 //   bank refresh  (amax per layer, then codes in both layouts from one pass)
 //   x amax        (per-tensor amax of the activations)
-//   x quantise    (codes of x in token-major and token-minor layouts, one read)
+//   x quantise    (codes of x, token-major)
 //   RoPE table, and the timeout self-test kernel.
 #include "kernels.cuh"
 
@@ -60,8 +60,8 @@ __device__ __forceinline__ const uint16_t* bank_row(const BankArgs& a, int l, in
   return a.Wv[l] + static_cast<int64_t>(n - 2 * a.Nq) * a.D;
 }
 
-// grid: (kBankAmaxBlocks, L), 256 threads.
-__global__ void __launch_bounds__(256) bank_amax_kernel(const __grid_constant__ BankArgs a, float* partials) {
+// grid: (kBankAmaxBlocks, L), 1024 threads.
+__global__ void __launch_bounds__(1024) bank_amax_kernel(const __grid_constant__ BankArgs a, float* partials) {
   __shared__ float red[32];
   const int l = blockIdx.y;
   const int row_chunks = a.D / 8;  // 16-byte chunks per row
@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__
   const int n0 = (blockIdx.x / tiles_d) * 128, d0 = (blockIdx.x % tiles_d) * 128;
   const float amax = block_reduce_partials(partials + l * kBankAmaxBlocks, kBankAmaxBlocks, red);
   const float s = scale_from_amax(amax);
+  const float rs = __frcp_rn(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) a.w_scale[l] = s;
 
   const int r = threadIdx.x >> 1;          // tile row
@@ -104,7 +105,8 @@ __global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__
       uint32_t c[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        c[q] = quant4(bf16_lo(w[2 * q]), bf16_hi(w[2 * q]), bf16_lo(w[2 * q + 1]), bf16_hi(w[2 * q + 1]), s);
+        c[q] = quant4_fast(bf16_lo(w[2 * q]), bf16_hi(w[2 * q]), bf16_lo(w[2 * q + 1]), bf16_hi(w[2 * q + 1]), s,
+                           rs);
       *reinterpret_cast<uint4*>(W8 + static_cast<int64_t>(n) * a.D + d0 + ch + j * 8) =
           make_uint4(c[0], c[1], c[2], c[3]);
 #pragma unroll
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__
 }
 
 cudaError_t launch_bank_amax(const BankArgs& a, float* partials, cudaStream_t s) {
-  bank_amax_kernel<<<dim3(kBankAmaxBlocks, a.L), 256, 0, s>>>(a, partials);
+  bank_amax_kernel<<<dim3(kBankAmaxBlocks, a.L), 1024, 0, s>>>(a, partials);
   return cudaGetLastError();
 }
 
@@ -144,97 +146,42 @@ cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStre
 }
 
 // ---------------------------------------------------------------------------
-// x -> x8 [T, D] and x8T [D, Tp] from one read.  Tile: 128 tokens x 128
-// columns, loaded by TMA as two 64-column boxes with 128-byte swizzling.
-// Each thread owns one token row: it reads its 128 values without bank
-// conflicts, writes 128 codes into the token-major staging tile (128-byte
-// swizzle) and one byte per column into the column-major staging tile.  Both
-// tiles leave by TMA.  Rows past T are zero-filled by TMA and so produce zero
-// codes in the padding columns of x8T; the x8 store is clipped at T.
-// grid: (Tp/128, D/128), 128 threads.
+// x -> x8 [T, D] codes.  Every block first re-reduces the amax partials of
+// x (a few KB from L2), then converts 16 values per thread per step: two
+// 16-byte loads, one 16-byte store.  T * D is a multiple of 16 (D % 128 == 0).
 // ---------------------------------------------------------------------------
-constexpr int kXQuantSmem = 1024 + 32768 + 16384 + 16384;
-
-__global__ void __launch_bounds__(128) x_quant_kernel(const __grid_constant__ CUtensorMap tm_x,
-                                                      const __grid_constant__ CUtensorMap tm_x8,
-                                                      const __grid_constant__ CUtensorMap tm_x8t,
-                                                      const float* partials, int nparts, float* x_scale,
-                                                      DevStatus st) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sx = smem;            // 2 x 16 KB: bf16 [128 rows][64 cols], 128-byte swizzle
-  uint8_t* s8 = smem + 32768;    // 16 KB: codes [128 tokens][128 cols], 128-byte swizzle
-  uint8_t* s8t = smem + 49152;   // 16 KB: codes [128 cols][128 tokens], 128-byte swizzle
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ float red[32];
-  __shared__ int abort_flag;
-
-  const int t0 = blockIdx.x * 128, d0 = blockIdx.y * 128;
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&bar, 32768);
-    tma_load_2d(sx, &tm_x, &bar, d0, t0);
-    tma_load_2d(sx + 16384, &tm_x, &bar, d0 + 64, t0);
-  }
-  const float amax = block_reduce_partials(partials, nparts, red);
-  const float s = scale_from_amax(amax);
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *x_scale = s;
-  const bool ok = mbar_wait(&bar, 0, &abort_flag, st, KID_X_QUANT);
-
-  const int r = threadIdx.x;
-  if (ok) {
+__device__ __forceinline__ uint4 quant16(uint4 u0, uint4 u1, float s, float rs) {
+  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  uint32_t q[4];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint8_t* rowp = sx + half * 16384 + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; c += 2) {  // two 16-byte chunks = 16 values = 16 codes
-        const uint4 u0 = *reinterpret_cast<const uint4*>(rowp + ((c ^ (r & 7)) << 4));
-        const uint4 u1 = *reinterpret_cast<const uint4*>(rowp + (((c + 1) ^ (r & 7)) << 4));
-        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          q[j] = quant4(bf16_lo(w[2 * j]), bf16_hi(w[2 * j]), bf16_lo(w[2 * j + 1]), bf16_hi(w[2 * j + 1]), s);
-        const int col0 = half * 64 + c * 8;  // first column of these 16 codes
-        const int chunk = col0 >> 4;         // 16-byte chunk of the code row
-        *reinterpret_cast<uint4*>(s8 + r * 128 + ((chunk ^ (r & 7)) << 4)) = make_uint4(q[0], q[1], q[2], q[3]);
-#pragma unroll
-        for (int b = 0; b < 16; ++b) {
-          const int col = col0 + b;
-          s8t[col * 128 + (((r >> 4) ^ (col & 7)) << 4) + (r & 15)] =
-              static_cast<uint8_t>(q[b >> 2] >> (8 * (b & 3)));
-        }
-      }
-    }
-  }
-  fence_async_smem();
-  __syncthreads();
-  if (threadIdx.x == 0 && ok) {
-    tma_store_2d(&tm_x8, s8, d0, t0);
-    tma_store_2d(&tm_x8t, s8t, t0, d0);
-    bulk_commit();
-    bulk_wait_all<0>();
-  }
+  for (int j = 0; j < 4; ++j)
+    q[j] = quant4_fast(bf16_lo(w[2 * j]), bf16_hi(w[2 * j]), bf16_lo(w[2 * j + 1]), bf16_hi(w[2 * j + 1]), s, rs);
+  return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
-cudaError_t launch_x_quant(const CUtensorMap& tm_x, const CUtensorMap& tm_x8, const CUtensorMap& tm_x8t, int Tp,
-                           int D, const float* partials, int nparts, float* x_scale, DevStatus st,
-                           cudaStream_t s) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(x_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXQuantSmem);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+__global__ void __launch_bounds__(256) x_quant_kernel(const uint16_t* __restrict__ x, int64_t n16,
+                                                      uint8_t* __restrict__ x8, const float* partials, int nparts,
+                                                      float* x_scale) {
+  __shared__ float red[32];
+  const float s = scale_from_amax(block_reduce_partials(partials, nparts, red));
+  const float rs = __frcp_rn(s);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *x_scale = s;
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  uint4* dst = reinterpret_cast<uint4*>(x8);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + stride < n16; i += 2 * stride) {  // two independent groups in flight
+    const uint4 a0 = __ldg(src + 2 * i), a1 = __ldg(src + 2 * i + 1);
+    const uint4 b0 = __ldg(src + 2 * (i + stride)), b1 = __ldg(src + 2 * (i + stride) + 1);
+    dst[i] = quant16(a0, a1, s, rs);
+    dst[i + stride] = quant16(b0, b1, s, rs);
   }
-  x_quant_kernel<<<dim3(Tp / 128, D / 128), 128, kXQuantSmem, s>>>(tm_x, tm_x8, tm_x8t, partials, nparts,
-                                                                   x_scale, st);
+  for (; i < n16; i += stride) dst[i] = quant16(__ldg(src + 2 * i), __ldg(src + 2 * i + 1), s, rs);
+}
+
+cudaError_t launch_x_quant(const uint16_t* x, int64_t n, uint8_t* x8, const float* partials, int nparts,
+                           float* x_scale, int blocks, cudaStream_t s) {
+  x_quant_kernel<<<blocks, 256, 0, s>>>(x, n / 16, x8, partials, nparts, x_scale);
   return cudaGetLastError();
 }
 

@@ -36,8 +36,6 @@
  *
  * Shapes: T tokens, D model width (multiple of 128), H heads, d_qk in
  * {64, 96, 128}, d_v = 128, N = H * (2*d_qk + d_v) packed rows.
- * Tp = qkvp_padded_tokens(T) (T rounded up to 128) is the leading dimension
- * of the token-minor FP8 layouts.
  */
 #ifndef QKVP_H_
 #define QKVP_H_
@@ -70,11 +68,6 @@ typedef struct qkvp_dims {
 
 /* Human-readable name of a qkvp_status value (static string, never NULL). */
 const char* qkvp_status_string(int status);
-
-/* T rounded up to a multiple of 128: the leading dimension of x8T and dY8T,
- * whose padding columns [T, Tp) the library fills with zero codes.  -1 if
- * T < 1. */
-int64_t qkvp_padded_tokens(int T);
 
 /* Bytes of scratch that qkvp_forward and qkvp_backward need for `dims`
  * (one workspace serves both).  0 if dims are unsupported.  The workspace
@@ -154,9 +147,8 @@ int qkvp_quantize_bank_static(int L, int D, int H, int d_qk, int d_v,
  *   q, k      out [H, T, d_qk] bf16
  *   v         out [H, T, d_v] bf16
  *   rstd      out [2, H, T] float32: 1/sqrt(mean(Y^2)+eps) of q (0) and k (1)
- *   x8        out [T, D] codes (the GEMM operand)
- *   x8T       out [D, Tp] codes, transpose of x8, zero in columns >= T
- *               (saved for the dW GEMM of the backward)
+ *   x8        out [T, D] codes: the GEMM operand, saved for the dW GEMM of
+ *               the backward (which reads it token-major, MN-major operand)
  *   x_scale   out [1] float32
  *   ws        scratch, qkvp_workspace_bytes(dims) bytes                    */
 int qkvp_forward(const qkvp_dims* dims, float eps,
@@ -164,24 +156,23 @@ int qkvp_forward(const qkvp_dims* dims, float eps,
                  const uint16_t* x, const int32_t* pos,
                  const uint8_t* W8, const float* w_scale,
                  uint16_t* q, uint16_t* k, uint16_t* v, float* rstd,
-                 uint8_t* x8, uint8_t* x8T, float* x_scale,
+                 uint8_t* x8, float* x_scale,
                  void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of the forward above ("Track 1 ... packed FP8 attention", sections
  * "Changes" and "Speed": FP8 backward using the cached transposed bank).
  * y is rebuilt from the saved outputs, y = RoPE^T(q), and
  * dY_q = rstd * RoPE^T(dq - q * mean(dq * q)) (the same for k), dY_v = dv;
- * dY is quantised with its own scale into dY8/dY8T, then
- *   dx = (dY8 . W8) * s_dy * s_w   via W8T as the K-major operand
- *   dW = (dY8^T . x8) * s_dy * s_x via dY8T and x8T
+ * dY is quantised with its own scale into dY8, then
+ *   dx = (dY8 . W8) * s_dy * s_w   with the cached W8T as the K-major operand
+ *   dW = (dY8^T . x8) * s_dy * s_x with dY8 and x8 read as MN-major operands
  *   dq, dk    in  [H, T, d_qk] bf16     dv in [H, T, d_v] bf16
  *   q, k      in  [H, T, d_qk] bf16 saved forward outputs
  *   rstd      in  [2, H, T] float32 saved forward output
  *   W8T       in  [D, N] codes of the layer, w_scale [1]
- *   x8T       in  [D, Tp] codes from the forward, x_scale [1]
+ *   x8        in  [T, D] codes from the forward, x_scale [1]
  *   dx        out [T, D] bf16           dW out [N, D] bf16 (overwritten)
- *   dY8       out [T, N] codes          dY8T out [N, Tp] codes (zero cols >= T)
- *   dy_scale  out [1] float32
+ *   dY8       out [T, N] codes          dy_scale out [1] float32
  *   ws        scratch, qkvp_workspace_bytes(dims) bytes                    */
 int qkvp_backward(const qkvp_dims* dims,
                   const float* rope_table, int max_pos,
@@ -189,9 +180,9 @@ int qkvp_backward(const qkvp_dims* dims,
                   const uint16_t* q, const uint16_t* k, const float* rstd,
                   const int32_t* pos,
                   const uint8_t* W8T, const float* w_scale,
-                  const uint8_t* x8T, const float* x_scale,
+                  const uint8_t* x8, const float* x_scale,
                   uint16_t* dx, uint16_t* dW,
-                  uint8_t* dY8, uint8_t* dY8T, float* dy_scale,
+                  uint8_t* dY8, float* dy_scale,
                   void* ws, size_t ws_bytes, void* stream);
 
 /* Diagnostic: launch one kernel that waits on a device barrier nothing ever

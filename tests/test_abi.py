@@ -51,12 +51,7 @@ def test_status_strings(qk):
     assert qk.lib().qkvp_status_string(99).decode() == "QKVP_ERR_UNKNOWN"
 
 
-def test_padded_tokens_and_workspace_sizes(qk):
-    assert qk.padded_tokens(1) == 128
-    assert qk.padded_tokens(128) == 128
-    assert qk.padded_tokens(129) == 256
-    assert qk.padded_tokens(49152) == 49152
-    assert qk.lib().qkvp_padded_tokens(0) == -1
+def test_workspace_sizes(qk):
     assert qk.workspace_bytes(qk.Shape(128, 768, 6)) > 0
     assert qk.workspace_bytes(qk.Shape(128, 768, 6, d_qk=80)) == 0      # unsupported width
     assert qk.workspace_bytes(qk.Shape(128, 700, 6)) == 0               # D not a multiple of 128
@@ -65,8 +60,8 @@ def test_padded_tokens_and_workspace_sizes(qk):
 
 
 def _fwd(qk, dims, ws_bytes=1 << 40, eps=1e-6, max_pos=128, ptr=4096, null_at=None):
-    # args[0] is the rope table, args[1:] the 12 tensor pointers x .. ws, in order
-    args = [ctypes.c_void_p(ptr) for _ in range(13)]
+    # args[0] is the rope table, args[1:] the 11 tensor pointers x .. ws, in order
+    args = [ctypes.c_void_p(ptr) for _ in range(12)]
     if null_at is not None:
         args[null_at] = None
     return qk.lib().qkvp_forward(ctypes.byref(dims), eps, args[0], max_pos, *args[1:], ws_bytes, None)
@@ -87,8 +82,8 @@ def test_forward_validation_codes(qk):
 
 def test_backward_validation_codes(qk):
     good = qk.Dims(200, 1024, 8, 128, 128)
-    # P[0] is the rope table, P[1:] the 17 tensor pointers dq .. ws, in order
-    P = [ctypes.c_void_p(8192) for _ in range(18)]
+    # P[0] is the rope table, P[1:] the 16 tensor pointers dq .. ws, in order
+    P = [ctypes.c_void_p(8192) for _ in range(17)]
     call = lambda dims, P, ws=1 << 40: qk.lib().qkvp_backward(ctypes.byref(dims), P[0], 64, *P[1:], ws, None)
     assert call(qk.Dims(200, 1024, 8, 100, 128), P) == qk.ERR_UNSUPPORTED
     bad = list(P)

@@ -43,10 +43,10 @@ def _run_forward(qk, s, seed=0):
     table = qk.build_rope_table(s.seq_len, s.d_qk, 10000.0, DEV)
     x, pos = inp["x"].to(DEV), inp["pos"].to(DEV)
     ws = qk.new_workspace(qk.Shape(s.T, s.D, s.H, s.d_qk, s.d_v), DEV)
-    q, k, v, saved, x8 = qk.forward(x, pos, W8, w_scale, s.H, table, s.d_qk, s.d_v, ws=ws)
+    q, k, v, saved = qk.forward(x, pos, W8, w_scale, s.H, table, s.d_qk, s.d_v, ws=ws)
     torch.cuda.synchronize()
     return dict(inp=inp, W8=W8, W8T=W8T, w_scale=w_scale, oW8=oW8, os_w=os_w, table=table, ws=ws,
-                q=q, k=k, v=v, saved=saved, x8=x8)
+                q=q, k=k, v=v, saved=saved, x8=saved.x8)
 
 
 SHAPES = [
@@ -114,9 +114,6 @@ def test_forward_matches_oracle(qk, s):
     fw = oracle.forward(f32(inp["x"]), r["oW8"], r["os_w"], inp["pos"].numpy(), s.H, s.d_qk, s.d_v)
     assert r["saved"].x_scale.item() == float(fw["x_scale"])
     np.testing.assert_array_equal(r["x8"].cpu().numpy(), fw["x8"])
-    x8T = r["saved"].x8T.cpu().numpy()
-    np.testing.assert_array_equal(x8T[:, :s.T], fw["x8"].T)
-    assert not x8T[:, s.T:].any(), "padding columns of x8T must hold zero codes"
     for name in ("q", "k", "v"):
         assert_close(f32(r[name]), fw[name], name)
     assert_close(r["saved"].rstd.cpu().numpy(), fw["rstd"], "rstd")
@@ -145,7 +142,7 @@ def _run_backward(qk, s, seed=0):
     k_saved = torch.from_numpy(fw["k"]).to(torch.bfloat16).contiguous()
     rstd_saved = torch.from_numpy(fw["rstd"]).to(torch.float32).contiguous()
     saved = qk.Saved(q=q_saved.to(DEV), k=k_saved.to(DEV), rstd=rstd_saved.to(DEV),
-                     x8T=r["saved"].x8T, x_scale=r["saved"].x_scale, pos=inp["pos"].to(DEV))
+                     x8=r["saved"].x8, x_scale=r["saved"].x_scale, pos=inp["pos"].to(DEV))
     out = qk.backward(*(g[n].to(DEV) for n in ("dq", "dk", "dv")), saved, r["W8T"], r["w_scale"], r["table"],
                       ws=r["ws"])
     torch.cuda.synchronize()
@@ -162,9 +159,6 @@ def test_backward_matches_oracle(qk, s):
     assert abs(dy_scale - float(bw["dy_scale"])) <= 1e-6 * float(bw["dy_scale"])
     dY8 = out["dY8"].cpu().numpy()
     assert_codes_match(dY8, bw["dY8"], "dY8")
-    dY8T = out["dY8T"].cpu().numpy()
-    np.testing.assert_array_equal(dY8T[:, :s.T], dY8.T)
-    assert not dY8T[:, s.T:].any(), "padding columns of dY8T must hold zero codes"
     # The GEMMs judged on the GPU's own codes: identical inputs, unique result.
     dX, dW = oracle.grad_gemms(dY8, np.float32(dy_scale), r["oW8"], r["os_w"], fw["x8"], fw["x_scale"])
     rank_one = s.T == 1      # dW is an outer product: see assert_close
@@ -193,7 +187,7 @@ def test_backward_deterministic(qk):
     s = synth.Shape(T=1000, D=768, H=6, seq_len=1000)
     a, _, _, _ = _run_backward(qk, s, seed=5)
     b, _, _, _ = _run_backward(qk, s, seed=5)
-    for name in ("dx", "dW", "dY8", "dY8T"):
+    for name in ("dx", "dW", "dY8"):
         assert torch.equal(a[name], b[name]), name
 
 
@@ -229,6 +223,6 @@ def test_binding_rejects_strided_tensors(qk):
     r = _run_forward(qk, s)
     g = synth.backward_inputs(s)
     bad = qk.Saved(q=r["q"].transpose(0, 1).contiguous().transpose(0, 1), k=r["k"], rstd=r["saved"].rstd,
-                   x8T=r["saved"].x8T, x_scale=r["saved"].x_scale, pos=r["saved"].pos)
+                   x8=r["saved"].x8, x_scale=r["saved"].x_scale, pos=r["saved"].pos)
     with pytest.raises(ValueError, match="contiguous"):
         qk.backward(*(g[n].to(DEV) for n in ("dq", "dk", "dv")), bad, r["W8T"], r["w_scale"], r["table"])

@@ -260,12 +260,17 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
 // that is the quotient's code; otherwise (q within 2^-20 of a rounding
 // boundary) the exact division decides.  For |q| below 2^-11 both ends and
 // the quotient give a signed zero of q's sign.
+// The rare exact path, kept out of line so the division is executed only when
+// a bracket straddles a rounding boundary (not predicated for every value).
+static __device__ __noinline__ uint32_t quant1_exact(float v, float s) { return quant1(v, s); }
+
 __device__ __forceinline__ uint32_t quant1_fast(float v, float s, float rs) {
   const float q = v * rs;
   const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
       make_float2(q * 0.99999904632568359375f, q * 1.00000095367431640625f), __NV_SATFINITE, __NV_E4M3);
   const uint32_t lo = c & 0xFFu, hi = (c >> 8) & 0xFFu;
-  return lo == hi ? lo : quant1(v, s);
+  if (__builtin_expect(lo == hi, 1)) return lo;
+  return quant1_exact(v, s);
 }
 __device__ __forceinline__ uint32_t quant4_fast(float a, float b, float c, float d, float s, float rs) {
   return quant1_fast(a, s, rs) | (quant1_fast(b, s, rs) << 8) | (quant1_fast(c, s, rs) << 16) |

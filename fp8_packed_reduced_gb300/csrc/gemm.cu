@@ -13,9 +13,10 @@
 //   warp 1     TMEM allocator and MMA issuer (one thread): 4 MMAs of K = 32
 //              per stage, commit to the stage's "empty" barrier, and to the
 //              accumulator's "full" barrier after the last stage of a unit
-//   warps 2-5  epilogue, one accumulator row (token) per thread; TMEM holds
-//              two 256-column accumulators so the epilogue of one unit
-//              overlaps the MMAs of the next
+//   warps 2-9  epilogue, two warps per TMEM lane quarter (each owning half of
+//              the unit's heads or columns), one accumulator row (token) per
+//              thread; TMEM holds two 256-column accumulators so the
+//              epilogue of one unit overlaps the MMAs of the next
 // Every wait is bounded (see mbar_wait); on expiry the kernel records
 // QKVP_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include "kernels.cuh"
@@ -26,9 +27,10 @@ constexpr int kBM = 128;                   // accumulator rows (tokens, or bank 
 constexpr int kBK = 128;                   // K bytes per stage (E4M3: 128 elements)
 constexpr int kAStage = kBM * kBK;         // 16 KB
 constexpr int kBStage = 256 * kBK;         // 32 KB (largest B tile)
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;             // 2 accumulators x 256 fp32 columns
-constexpr int kEpiWarpBytes = 16384;       // staging per epilogue warp: 8 boxes of 32 x 64 B
+constexpr int kEpiWarpBytes = 8192;        // staging per epilogue warp: 4 boxes of 32 rows x 64 B
 constexpr int kMaxStages = 6;
 
 struct Unit {
@@ -46,7 +48,7 @@ struct GemmSmem {
 };
 
 __host__ __device__ constexpr int gemm_smem_bytes(int stages, bool epi_staging) {
-  return 1024 + stages * (kAStage + kBStage) + (epi_staging ? 4 * kEpiWarpBytes : 0);
+  return 1024 + stages * (kAStage + kBStage) + (epi_staging ? kEpiWarps * kEpiWarpBytes : 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -144,7 +146,7 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&g.tfull[b], 1);
-      mbar_init(&g.tempty[b], 128);
+      mbar_init(&g.tempty[b], 32 * kEpiWarps);
     }
     mbar_init(&g.mma_done, 1);
     fence_mbar_init();
@@ -165,8 +167,9 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
   } else if (warp == 1) {
     if (lane == 0) mma_role(sc, sA, sB, g, tmem_base, stages, st, kid);
   } else {
-    const int qw = warp & 3;  // TMEM lane quarter this warp may access
-    epi.begin(qw, lane, sE + (warp - 2) * kEpiWarpBytes);
+    const int qw = warp & 3;          // TMEM lane quarter this warp may access
+    const int sub = (warp - 2) >> 2;  // which half of the unit's heads / columns
+    epi.begin(qw, sub, lane, sE + (warp - 2) * kEpiWarpBytes);
     int it = 0;
     for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x, ++it) {
       const int buf = it & 1;
@@ -265,25 +268,25 @@ struct FwdEpi {
   const CUtensorMap* tv;
   const DevStatus& st;
   uint8_t* stage;
-  int qw, lane, half;
+  int qw, sub, lane;
   float sxw;
 
-  __device__ void begin(int qw_, int lane_, uint8_t* stage_) {
+  __device__ void begin(int qw_, int sub_, int lane_, uint8_t* stage_) {
     qw = qw_;
+    sub = sub_;
     lane = lane_;
     stage = stage_;
-    half = 0;
     sxw = (*p.x_scale) * (*p.w_scale);
   }
   __device__ void finish() {
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
   }
-  // wait until the stores that last read staging half `half` are done
-  __device__ uint8_t* acquire_half() {
-    if (lane == 0) bulk_wait_read<1>();
+  // wait until the stores that last read this warp's staging boxes are done
+  __device__ uint8_t* acquire() {
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
-    return stage + half * 8192;
+    return stage;
   }
 
   __device__ void process(int u, uint32_t tacc) {
@@ -304,9 +307,9 @@ struct FwdEpi {
       }
     }
     const float2* rope = reinterpret_cast<const float2*>(p.rope);
-    for (int hh = 0; hh < nh; ++hh) {
+    for (int hh = sub; hh < nh; hh += 2) {  // this warp's heads of the unit
       const int h = head0 + hh;
-      uint8_t* buf = acquire_half();
+      uint8_t* buf = acquire();
       if (kind < 2) {
         uint32_t raw[DQK];
 #pragma unroll
@@ -370,7 +373,6 @@ struct FwdEpi {
           bulk_commit();
         }
       }
-      half ^= 1;
     }
   }
 };
@@ -412,10 +414,11 @@ struct DxEpi {
   const DxParams& p;
   const CUtensorMap* tdx;
   uint8_t* stage;
-  int qw, lane, ring;
+  int qw, sub, lane, ring;
   float sc;
-  __device__ void begin(int qw_, int lane_, uint8_t* stage_) {
+  __device__ void begin(int qw_, int sub_, int lane_, uint8_t* stage_) {
     qw = qw_;
+    sub = sub_;
     lane = lane_;
     stage = stage_;
     ring = 0;
@@ -428,9 +431,10 @@ struct DxEpi {
   __device__ void process(int u, uint32_t tacc) {
     const int m = u / p.n_tiles, j = u % p.n_tiles;
     const int ty = m * kBM + qw * 32;
-    for (int c0 = 0; c0 < p.bn; c0 += 32) {
-      uint8_t* slot = stage + (ring & 7) * 2048;
-      if (lane == 0) bulk_wait_read<7>();
+    const int half = p.bn / 2;   // this warp's columns: [sub * half, (sub + 1) * half)
+    for (int c0 = sub * half; c0 < (sub + 1) * half; c0 += 32) {
+      uint8_t* slot = stage + (ring & 3) * 2048;
+      if (lane == 0) bulk_wait_read<3>();
       __syncwarp();
       uint32_t raw[32];
       tmem_ld16(tacc + c0, raw);
@@ -497,16 +501,18 @@ struct DwSched {
 
 struct DwEpi {
   const DwParams& p;
-  int qw, lane;
-  __device__ void begin(int qw_, int lane_, uint8_t*) {
+  int qw, sub, lane;
+  __device__ void begin(int qw_, int sub_, int lane_, uint8_t*) {
     qw = qw_;
+    sub = sub_;
     lane = lane_;
   }
   __device__ void finish() {}
   __device__ void process(int u, uint32_t tacc) {
     // unit u owns partials[u][bn][128] (column-major tile): coalesced stores
     float* dst = p.partials + static_cast<int64_t>(u) * p.bn * kBM + qw * 32 + lane;
-    for (int c0 = 0; c0 < p.bn; c0 += 32) {
+    const int half = p.bn / 2;
+    for (int c0 = sub * half; c0 < (sub + 1) * half; c0 += 32) {
       uint32_t raw[32];
       tmem_ld16(tacc + c0, raw);
       tmem_ld16(tacc + c0 + 16, raw + 16);

@@ -27,8 +27,8 @@ constexpr int kBM = 128;                   // accumulator rows (tokens, or bank 
 constexpr int kBK = 128;                   // K bytes per stage (E4M3: 128 elements)
 constexpr int kAStage = kBM * kBK;         // 16 KB
 constexpr int kBStage = 256 * kBK;         // 32 KB (largest B tile)
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Threads of a GEMM CTA with EW epilogue warps (4 or 8).
+__host__ __device__ constexpr int gemm_threads(int ew) { return 64 + 32 * ew; }
 constexpr int kTmemCols = 512;             // 2 accumulators x 256 fp32 columns
 constexpr int kEpiWarpBytes = 8192;        // staging per epilogue warp: 4 boxes of 32 rows x 64 B
 constexpr int kMaxStages = 6;
@@ -47,8 +47,8 @@ struct GemmSmem {
   int abort_flag;
 };
 
-__host__ __device__ constexpr int gemm_smem_bytes(int stages, bool epi_staging) {
-  return 1024 + stages * (kAStage + kBStage) + (epi_staging ? kEpiWarps * kEpiWarpBytes : 0);
+__host__ __device__ constexpr int gemm_smem_bytes(int stages, int ew, bool epi_staging) {
+  return 1024 + stages * (kAStage + kBStage) + (epi_staging ? ew * kEpiWarpBytes : 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -127,7 +127,7 @@ __device__ void mma_role(const Sched& sc, uint8_t* sA, uint8_t* sB, GemmSmem& g,
 // ---------------------------------------------------------------------------
 // Common body
 // ---------------------------------------------------------------------------
-template <class Sched, class Epi>
+template <int EW, class Sched, class Epi>
 __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUtensorMap* tmA,
                                           const CUtensorMap* tmB, int stages, const DevStatus& st, int kid) {
   extern __shared__ uint8_t smem_raw[];
@@ -146,7 +146,7 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&g.tfull[b], 1);
-      mbar_init(&g.tempty[b], 32 * kEpiWarps);
+      mbar_init(&g.tempty[b], 32 * EW);
     }
     mbar_init(&g.mma_done, 1);
     fence_mbar_init();
@@ -168,8 +168,8 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
     if (lane == 0) mma_role(sc, sA, sB, g, tmem_base, stages, st, kid);
   } else {
     const int qw = warp & 3;          // TMEM lane quarter this warp may access
-    const int sub = (warp - 2) >> 2;  // which half of the unit's heads / columns
-    epi.begin(qw, sub, lane, sE + (warp - 2) * kEpiWarpBytes);
+    const int sub = (warp - 2) >> 2;  // which share of the unit's heads / columns
+    epi.begin(qw, sub, EW / 4, lane, sE + (warp - 2) * kEpiWarpBytes);
     int it = 0;
     for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x, ++it) {
       const int buf = it & 1;
@@ -268,12 +268,13 @@ struct FwdEpi {
   const CUtensorMap* tv;
   const DevStatus& st;
   uint8_t* stage;
-  int qw, sub, lane;
+  int qw, sub, nsub, lane;
   float sxw;
 
-  __device__ void begin(int qw_, int sub_, int lane_, uint8_t* stage_) {
+  __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t* stage_) {
     qw = qw_;
     sub = sub_;
+    nsub = nsub_;
     lane = lane_;
     stage = stage_;
     sxw = (*p.x_scale) * (*p.w_scale);
@@ -307,7 +308,7 @@ struct FwdEpi {
       }
     }
     const float2* rope = reinterpret_cast<const float2*>(p.rope);
-    for (int hh = sub; hh < nh; hh += 2) {  // this warp's heads of the unit
+    for (int hh = sub; hh < nh; hh += nsub) {  // this warp's heads of the unit
       const int h = head0 + hh;
       uint8_t* buf = acquire();
       if (kind < 2) {
@@ -377,15 +378,17 @@ struct FwdEpi {
   }
 };
 
+constexpr int kFwdEW = 4, kDxEW = 4, kDwEW = 8;
+
 template <int DQK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(kFwdEW), 1)
     fwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ FwdParams p, DevStatus st,
                     int stages) {
   FwdSched sc{p};
   FwdEpi<DQK> epi{p, sc, &tq, &tk, &tv, st};
-  gemm_body(sc, epi, &tmA, &tmB, stages, st, KID_FWD_GEMM);
+  gemm_body<kFwdEW>(sc, epi, &tmA, &tmB, stages, st, KID_FWD_GEMM);
 }
 
 // ---------------------------------------------------------------------------
@@ -414,11 +417,12 @@ struct DxEpi {
   const DxParams& p;
   const CUtensorMap* tdx;
   uint8_t* stage;
-  int qw, sub, lane, ring;
+  int qw, sub, nsub, lane, ring;
   float sc;
-  __device__ void begin(int qw_, int sub_, int lane_, uint8_t* stage_) {
+  __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t* stage_) {
     qw = qw_;
     sub = sub_;
+    nsub = nsub_;
     lane = lane_;
     stage = stage_;
     ring = 0;
@@ -431,8 +435,8 @@ struct DxEpi {
   __device__ void process(int u, uint32_t tacc) {
     const int m = u / p.n_tiles, j = u % p.n_tiles;
     const int ty = m * kBM + qw * 32;
-    const int half = p.bn / 2;   // this warp's columns: [sub * half, (sub + 1) * half)
-    for (int c0 = sub * half; c0 < (sub + 1) * half; c0 += 32) {
+    const int share = p.bn / nsub;   // this warp's columns: [sub * share, (sub + 1) * share)
+    for (int c0 = sub * share; c0 < (sub + 1) * share; c0 += 32) {
       uint8_t* slot = stage + (ring & 3) * 2048;
       if (lane == 0) bulk_wait_read<3>();
       __syncwarp();
@@ -459,13 +463,13 @@ struct DxEpi {
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(kDxEW), 1)
     dx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tdx, const __grid_constant__ DxParams p, DevStatus st,
                    int stages) {
   DxSched sc{p};
   DxEpi epi{p, &tdx};
-  gemm_body(sc, epi, &tmA, &tmB, stages, st, KID_DX_GEMM);
+  gemm_body<kDxEW>(sc, epi, &tmA, &tmB, stages, st, KID_DX_GEMM);
 }
 
 // ---------------------------------------------------------------------------
@@ -501,18 +505,19 @@ struct DwSched {
 
 struct DwEpi {
   const DwParams& p;
-  int qw, sub, lane;
-  __device__ void begin(int qw_, int sub_, int lane_, uint8_t*) {
+  int qw, sub, nsub, lane;
+  __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t*) {
     qw = qw_;
     sub = sub_;
+    nsub = nsub_;
     lane = lane_;
   }
   __device__ void finish() {}
   __device__ void process(int u, uint32_t tacc) {
     // unit u owns partials[u][bn][128] (column-major tile): coalesced stores
     float* dst = p.partials + static_cast<int64_t>(u) * p.bn * kBM + qw * 32 + lane;
-    const int half = p.bn / 2;
-    for (int c0 = sub * half; c0 < (sub + 1) * half; c0 += 32) {
+    const int share = p.bn / nsub;
+    for (int c0 = sub * share; c0 < (sub + 1) * share; c0 += 32) {
       uint32_t raw[32];
       tmem_ld16(tacc + c0, raw);
       tmem_ld16(tacc + c0 + 16, raw + 16);
@@ -523,12 +528,12 @@ struct DwEpi {
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(kDwEW), 1)
     dw_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ DwParams p, DevStatus st, int stages) {
   DwSched sc{p};
   DwEpi epi{p};
-  gemm_body(sc, epi, &tmA, &tmB, stages, st, KID_DW_GEMM);
+  gemm_body<kDwEW>(sc, epi, &tmA, &tmB, stages, st, KID_DW_GEMM);
 }
 
 // dW[n][d] = bf16(s_dy * s_x * sum over splits, in split order, of the
@@ -562,7 +567,7 @@ __global__ void __launch_bounds__(256) dw_reduce_kernel(const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
-constexpr int kFwdStages = 3, kDxStages = 3, kDwStages = 4;
+constexpr int kFwdStages = 4, kDxStages = 4, kDwStages = 4;
 
 template <class K>
 static cudaError_t set_smem_once(K kernel, int bytes, bool (&done)[64]) {
@@ -580,10 +585,10 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, 
                                 const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
                                 DevStatus st, cudaStream_t s) {
   static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kFwdStages, true);
+  const int smem = gemm_smem_bytes(kFwdStages, kFwdEW, true);
   cudaError_t e = set_smem_once(fwd_gemm_kernel<DQK>, smem, done);
   if (e != cudaSuccess) return e;
-  fwd_gemm_kernel<DQK><<<grid, kThreads, smem, s>>>(tmA, tmB, tq, tk, tv, p, st, kFwdStages);
+  fwd_gemm_kernel<DQK><<<grid, gemm_threads(kFwdEW), smem, s>>>(tmA, tmB, tq, tk, tv, p, st, kFwdStages);
   return cudaGetLastError();
 }
 
@@ -601,20 +606,20 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
                            const DxParams& p, int grid, DevStatus st, cudaStream_t s) {
   static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kDxStages, true);
+  const int smem = gemm_smem_bytes(kDxStages, kDxEW, true);
   cudaError_t e = set_smem_once(dx_gemm_kernel, smem, done);
   if (e != cudaSuccess) return e;
-  dx_gemm_kernel<<<grid, kThreads, smem, s>>>(tmA, tmB, tdx, p, st, kDxStages);
+  dx_gemm_kernel<<<grid, gemm_threads(kDxEW), smem, s>>>(tmA, tmB, tdx, p, st, kDxStages);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int grid,
                            DevStatus st, cudaStream_t s) {
   static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kDwStages, false);
+  const int smem = gemm_smem_bytes(kDwStages, kDwEW, false);
   cudaError_t e = set_smem_once(dw_gemm_kernel, smem, done);
   if (e != cudaSuccess) return e;
-  dw_gemm_kernel<<<grid, kThreads, smem, s>>>(tmA, tmB, p, st, kDwStages);
+  dw_gemm_kernel<<<grid, gemm_threads(kDwEW), smem, s>>>(tmA, tmB, p, st, kDwStages);
   return cudaGetLastError();
 }
 

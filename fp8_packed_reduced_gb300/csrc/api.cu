@@ -135,8 +135,10 @@ struct TimingHook {
   int n = 0, next = 0;
 } g_timing;
 
+// Recorded as an external event node when the stream is being captured into
+// a CUDA graph, so the graph's launches record it too.
 void mark(cudaStream_t s) {
-  if (g_timing.next < g_timing.n) cudaEventRecord(g_timing.ev[g_timing.next++], s);
+  if (g_timing.next < g_timing.n) cudaEventRecordWithFlags(g_timing.ev[g_timing.next++], s, cudaEventRecordExternal);
 }
 
 #define QKVP_TRY_CUDA(expr)                          \

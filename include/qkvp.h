@@ -198,7 +198,8 @@ int qkvp_set_wait_timeout_ns(uint64_t ns);
 /* Kernel timing hook.  Arms `n` (<= 256) caller-created cudaEvent_t handles
  * (HOST array, not copied beyond the handles themselves).  While armed, the
  * calls above record the next unused event on their stream before their
- * first kernel and after each kernel, so consecutive events bracket one
+ * first kernel and after each kernel (as external event nodes when the stream
+ * is being captured into a CUDA graph), so consecutive events bracket one
  * kernel each.  Order of the kernels: qkvp_quantize_bank: amax, quantise;
  * qkvp_forward: x amax, x quantise, forward GEMM; qkvp_backward: dY amax,
  * dY quantise, dX GEMM, dW GEMM, dW reduction.  n = 0 disarms.  Not

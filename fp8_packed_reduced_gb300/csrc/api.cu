@@ -284,9 +284,16 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   float* xparts = reinterpret_cast<float*>(wsb + kStatusBytes);
   const DevStatus st = dev_status(ws);
 
+  // Tiles of the packed GEMM cover whole heads: q/k tiles of hq heads (the
+  // last one may hold fewer), v tiles of 2 heads.  B is loaded in boxes of the
+  // largest height (<= 256) that divides every tile width.
+  const int hq = dqk == 64 ? 4 : 2;
+  int b_rows = 256;
+  for (int w : {hq * dqk, (H % hq) * dqk, 2 * dv, (H % 2) * dv})
+    while (w > 0 && w % b_rows != 0) b_rows /= 2;
   CUtensorMap tm_x8, tm_w, tm_q, tm_k, tm_v;
   bool ok = map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map3d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -305,7 +312,8 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.H = H;
   p.d_qk = dqk;
   p.d_v = dv;
-  p.hq = dqk == 64 ? 4 : 2;
+  p.hq = hq;
+  p.b_rows = b_rows;
   p.nq = (H + p.hq - 1) / p.hq;
   p.nv = (H + 1) / 2;
   p.n_tiles = 2 * p.nq + p.nv;
@@ -362,7 +370,8 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   // dY8 [T, N] read as 128 x 128 tiles: K-major A of the dX GEMM, MN-major A of the dW GEMM
   CUtensorMap tm_dy, tm_w8t, tm_dx, tm_x8;
   ok = ok && map2d(&tm_dy, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_w8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8T, N, D, N, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  const int dx_bn = D % 256 == 0 ? 256 : 128;   // one box per stage: the whole B tile
+  ok = ok && map2d(&tm_w8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8T, N, D, N, 128, dx_bn, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dx, D, T, D * 2ull, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return QKVP_ERR_CUDA;
@@ -391,7 +400,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   DxParams xp;
   xp.T = T;
   xp.D = D;
-  xp.bn = D % 256 == 0 ? 256 : 128;
+  xp.bn = dx_bn;
   xp.n_tiles = D / xp.bn;
   xp.num_units = tiles * xp.n_tiles;
   xp.kblocks = (N + 127) / 128;

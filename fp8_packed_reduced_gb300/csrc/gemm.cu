@@ -203,11 +203,13 @@ __device__ __forceinline__ void stage16(uint8_t* boxes, int row, int c0, const u
 }
 
 // K-major operands: A is one box of 128 rows x 128 bytes of K at (k, a_row);
-// B is ncols/32 boxes of 32 rows x 128 bytes at (k, b_row + 32 j).
+// B is ncols/R boxes of R rows x 128 bytes at (k, b_row + R j), R = b_rows
+// (the B tensor map's box height).
 __device__ __forceinline__ void load_k_major(const Unit& ui, int kb, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                             uint8_t* sA, uint8_t* sB, uint64_t* bar) {
+                                             uint8_t* sA, uint8_t* sB, uint64_t* bar, int b_rows) {
   tma_load_2d(sA, tmA, bar, kb * kBK, ui.a_row);
-  for (int j = 0; j < ui.ncols / 32; ++j) tma_load_2d(sB + j * 32 * kBK, tmB, bar, kb * kBK, ui.b_row + 32 * j);
+  for (int j = 0; j < ui.ncols / b_rows; ++j)
+    tma_load_2d(sB + j * b_rows * kBK, tmB, bar, kb * kBK, ui.b_row + b_rows * j);
 }
 
 // ---------------------------------------------------------------------------
@@ -218,7 +220,7 @@ struct FwdSched {
   const FwdParams& p;
   __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
                        uint8_t* sB, uint64_t* bar) const {
-    load_k_major(ui, kb, a, b, sA, sB, bar);
+    load_k_major(ui, kb, a, b, sA, sB, bar, p.b_rows);
   }
   __device__ int num_units() const { return p.num_units; }
   // kind 0 = q, 1 = k, 2 = v
@@ -399,7 +401,7 @@ struct DxSched {
   const DxParams& p;
   __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
                        uint8_t* sB, uint64_t* bar) const {
-    load_k_major(ui, kb, a, b, sA, sB, bar);
+    load_k_major(ui, kb, a, b, sA, sB, bar, p.bn);
   }
   __device__ int num_units() const { return p.num_units; }
   __device__ Unit unit(int u) const {

@@ -48,6 +48,7 @@ struct FwdParams {
   int n_tiles;       // 2*nq + nv
   int num_units;     // ceil(T/128) * n_tiles
   int kblocks;       // D / 128
+  int b_rows;        // box height of the W8 tensor map (divides every tile's width)
   float eps;
   const float* x_scale;
   const float* w_scale;

@@ -285,15 +285,13 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   const DevStatus st = dev_status(ws);
 
   // Tiles of the packed GEMM cover whole heads: q/k tiles of hq heads (the
-  // last one may hold fewer), v tiles of 2 heads.  B is loaded in boxes of the
-  // largest height (<= 256) that divides every tile width.
+  // last one may hold fewer), v tiles of 2 heads.  Each stage loads B as one
+  // box of the full tile height: hq*d_qk rows (q/k) or 2*d_v rows (v).
   const int hq = dqk == 64 ? 4 : 2;
-  int b_rows = 256;
-  for (int w : {hq * dqk, (H % hq) * dqk, 2 * dv, (H % 2) * dv})
-    while (w > 0 && w % b_rows != 0) b_rows /= 2;
-  CUtensorMap tm_x8, tm_w, tm_q, tm_k, tm_v;
+  CUtensorMap tm_x8, tm_w, tm_wv, tm_q, tm_k, tm_v;
   bool ok = map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, hq * dqk, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, 2 * dv, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map3d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -313,7 +311,6 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.d_qk = dqk;
   p.d_v = dv;
   p.hq = hq;
-  p.b_rows = b_rows;
   p.nq = (H + p.hq - 1) / p.hq;
   p.nv = (H + 1) / 2;
   p.n_tiles = 2 * p.nq + p.nv;
@@ -327,7 +324,7 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.pos = pos;
   p.rstd = rstd;
   const int grid = std::min(p.num_units, sms);
-  QKVP_TRY_CUDA(launch_fwd_gemm(tm_x8, tm_w, tm_q, tm_k, tm_v, p, grid, st, s));
+  QKVP_TRY_CUDA(launch_fwd_gemm(tm_x8, tm_w, tm_wv, tm_q, tm_k, tm_v, p, grid, st, s));
   mark(s);
   return QKVP_OK;
 }

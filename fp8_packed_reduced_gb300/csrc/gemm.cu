@@ -35,6 +35,8 @@ constexpr int kMaxStages = 6;
 
 struct Unit {
   int a_row, b_row, ncols, kb0, kb1;
+  int b_bytes;   // bytes the B loads of one stage deliver (>= ncols * 128)
+  int b_sel;     // which B tensor map the schedule loads from (forward: 0 q/k, 1 v)
 };
 
 struct GemmSmem {
@@ -64,7 +66,7 @@ __device__ void producer_role(const Sched& sc, const CUtensorMap* tmA, const CUt
     const Unit ui = sc.unit(u);
     for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
       if (!mbar_wait(&g.empty[stage], phase ^ 1, &g.abort_flag, st, kid)) goto drain;
-      mbar_arrive_expect_tx(&g.full[stage], static_cast<uint32_t>(kAStage + ui.ncols * kBK));
+      mbar_arrive_expect_tx(&g.full[stage], static_cast<uint32_t>(kAStage + ui.b_bytes));
       sc.load(ui, kb, tmA, tmB, sA + stage * kAStage, sB + stage * kBStage, &g.full[stage]);
       used |= 1u << stage;
       last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -218,9 +220,13 @@ __device__ __forceinline__ void load_k_major(const Unit& ui, int kb, const CUten
 struct FwdSched {
   static constexpr bool kMN = false;
   const FwdParams& p;
+  const CUtensorMap* tmBv;   // W8 with the v tiles' box height (the q/k one is the body's B map)
+  // B: one box per stage, hq*d_qk rows for q/k tiles and 2*d_v rows for v
+  // tiles (a narrower last tile receives the whole box; the MMA uses ncols).
   __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
                        uint8_t* sB, uint64_t* bar) const {
-    load_k_major(ui, kb, a, b, sA, sB, bar, p.b_rows);
+    tma_load_2d(sA, a, bar, kb * kBK, ui.a_row);
+    tma_load_2d(sB, ui.b_sel == 0 ? b : tmBv, bar, kb * kBK, ui.b_row);
   }
   __device__ int num_units() const { return p.num_units; }
   // kind 0 = q, 1 = k, 2 = v
@@ -248,12 +254,18 @@ struct FwdSched {
     if (kind == 0) {
       r.b_row = head0 * p.d_qk;
       r.ncols = nh * p.d_qk;
+      r.b_bytes = p.hq * p.d_qk * kBK;
+      r.b_sel = 0;
     } else if (kind == 1) {
       r.b_row = p.H * p.d_qk + head0 * p.d_qk;
       r.ncols = nh * p.d_qk;
+      r.b_bytes = p.hq * p.d_qk * kBK;
+      r.b_sel = 0;
     } else {
       r.b_row = 2 * p.H * p.d_qk + head0 * p.d_v;
       r.ncols = nh * p.d_v;
+      r.b_bytes = 2 * p.d_v * kBK;
+      r.b_sel = 1;
     }
     r.kb0 = 0;
     r.kb1 = p.kblocks;
@@ -385,10 +397,11 @@ constexpr int kFwdEW = 4, kDxEW = 4, kDwEW = 8;
 template <int DQK>
 __global__ void __launch_bounds__(gemm_threads(kFwdEW), 1)
     fwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmBv,
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ FwdParams p, DevStatus st,
                     int stages) {
-  FwdSched sc{p};
+  FwdSched sc{p, &tmBv};
   FwdEpi<DQK> epi{p, sc, &tq, &tk, &tv, st};
   gemm_body<kFwdEW>(sc, epi, &tmA, &tmB, stages, st, KID_FWD_GEMM);
 }
@@ -409,6 +422,8 @@ struct DxSched {
     r.a_row = (u / p.n_tiles) * kBM;
     r.b_row = (u % p.n_tiles) * p.bn;
     r.ncols = p.bn;
+    r.b_bytes = p.bn * kBK;
+    r.b_sel = 0;
     r.kb0 = 0;
     r.kb1 = p.kblocks;
     return r;
@@ -499,6 +514,8 @@ struct DwSched {
     r.a_row = (tile / p.n_tiles) * kBM;
     r.b_row = (tile % p.n_tiles) * p.bn;
     r.ncols = p.bn;
+    r.b_bytes = p.bn * kBK;
+    r.b_sel = 0;
     r.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks_total / p.splits);
     r.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks_total / p.splits);
     return r;
@@ -583,24 +600,25 @@ static cudaError_t set_smem_once(K kernel, int bytes, bool (&done)[64]) {
 }
 
 template <int DQK>
-static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tq,
+static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
+                                const CUtensorMap& tq,
                                 const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
                                 DevStatus st, cudaStream_t s) {
   static bool done[64] = {};
   const int smem = gemm_smem_bytes(kFwdStages, kFwdEW, true);
   cudaError_t e = set_smem_once(fwd_gemm_kernel<DQK>, smem, done);
   if (e != cudaSuccess) return e;
-  fwd_gemm_kernel<DQK><<<grid, gemm_threads(kFwdEW), smem, s>>>(tmA, tmB, tq, tk, tv, p, st, kFwdStages);
+  fwd_gemm_kernel<DQK><<<grid, gemm_threads(kFwdEW), smem, s>>>(tmA, tmB, tmBv, tq, tk, tv, p, st, kFwdStages);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tq,
-                            const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
-                            DevStatus st, cudaStream_t s) {
+cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
+                            const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                            int grid, DevStatus st, cudaStream_t s) {
   switch (p.d_qk) {
-    case 64: return launch_fwd_t<64>(tmA, tmB, tq, tk, tv, p, grid, st, s);
-    case 96: return launch_fwd_t<96>(tmA, tmB, tq, tk, tv, p, grid, st, s);
-    case 128: return launch_fwd_t<128>(tmA, tmB, tq, tk, tv, p, grid, st, s);
+    case 64: return launch_fwd_t<64>(tmA, tmB, tmBv, tq, tk, tv, p, grid, st, s);
+    case 96: return launch_fwd_t<96>(tmA, tmB, tmBv, tq, tk, tv, p, grid, st, s);
+    case 128: return launch_fwd_t<128>(tmA, tmB, tmBv, tq, tk, tv, p, grid, st, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -48,7 +48,6 @@ struct FwdParams {
   int n_tiles;       // 2*nq + nv
   int num_units;     // ceil(T/128) * n_tiles
   int kblocks;       // D / 128
-  int b_rows;        // box height of the W8 tensor map (divides every tile's width)
   float eps;
   const float* x_scale;
   const float* w_scale;
@@ -69,9 +68,10 @@ struct DwParams {
   float* partials;    // [splits][m_tiles][n_tiles][bn][128] float32
 };
 
-cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tq,
-                            const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
-                            DevStatus st, cudaStream_t s);
+// tmB / tmBv: W8 with box heights hq*d_qk (q/k tiles) and 2*d_v (v tiles).
+cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
+                            const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                            int grid, DevStatus st, cudaStream_t s);
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
                            const DxParams& p, int grid, DevStatus st, cudaStream_t s);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int grid,

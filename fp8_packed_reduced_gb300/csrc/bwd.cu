@@ -83,32 +83,29 @@ __device__ __forceinline__ float row_mean_dot(const uint8_t* in0, const uint8_t*
 // into a[] and [HALF+16g, HALF+16g+16) into b[].
 template <int DQK>
 __device__ __forceinline__ void dy_group(const uint8_t* in0, const uint8_t* in1, int r, float mu, float rstd,
-                                         const float2* rope_row, int max_pos, int g, float (&a)[16],
-                                         float (&b)[16]) {
+                                         const float2 (&cs)[DQK / 2], int g, float (&a)[16], float (&b)[16]) {
   constexpr int HALF = DQK / 2;
   float ga[16], gb[16], oa[16], ob[16];
   load16(in0, r, g * 16, ga);
   load16(in0, r, HALF + g * 16, gb);
   load16(in1, r, g * 16, oa);
   load16(in1, r, HALF + g * 16, ob);
-  const float2* cs_ptr = rope_row + static_cast<int64_t>(g * 16) * max_pos;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float ua = ga[j] - mu * oa[j];
     const float ub = gb[j] - mu * ob[j];
-    const float2 cs = __ldg(cs_ptr + static_cast<int64_t>(j) * max_pos);
-    a[j] = rstd * (ua * cs.x + ub * cs.y);
-    b[j] = rstd * (ub * cs.x - ua * cs.y);
+    const float2 c = cs[g * 16 + j];
+    a[j] = rstd * (ua * c.x + ub * c.y);
+    b[j] = rstd * (ub * c.x - ua * c.y);
   }
 }
 
 // Codes of 16 consecutive columns [c0, c0+16) of row r into the token-major
 // staging boxes [128 rows][32 codes].
-__device__ __forceinline__ void emit16(const float (&v)[16], float s, float rs, int r, int c0, uint8_t* out8) {
+__device__ __forceinline__ void emit16(const float (&v)[16], const Bracket& k, int r, int c0, uint8_t* out8) {
   uint32_t w[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    w[q] = quant4_fast(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], s, rs);
+  for (int q = 0; q < 4; ++q) w[q] = quant4_fast(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], k);
   *reinterpret_cast<uint4*>(out8 + (c0 >> 5) * kOutBox + r * 32 + (c0 & 31)) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -168,10 +165,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   __syncthreads();
 
-  float s_dy = 1.f, rs_dy = 1.f;
+  Bracket kq{1.f, 1.f, 1.f};
   if (QUANT) {
-    s_dy = scale_from_amax(block_reduce_partials(p.partials, p.nparts, red));
-    rs_dy = __frcp_rn(s_dy);
+    const float s_dy = scale_from_amax(block_reduce_partials(p.partials, p.nparts, red));
+    kq = make_bracket(s_dy);
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.dy_scale = s_dy;
   }
 
@@ -214,7 +211,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool valid = t < p.T;
       float rstd;
       int pos;
-      if (b.part < 2) row_state(p, b, t, rstd, pos, st, kid);
+      float2 cs[DQK / 2];  // this row's cos/sin, loaded before the inputs arrive
+      if (b.part < 2) {
+        row_state(p, b, t, rstd, pos, st, kid);
+        const float2* rope_row = rope + pos;
+#pragma unroll
+        for (int i = 0; i < DQK / 2; ++i) cs[i] = __ldg(rope_row + static_cast<int64_t>(i) * p.max_pos);
+      }
       if (QUANT) {
         // the previous unit's stores have read this group's staging tiles
         if (r == 0) bulk_wait_read<0>();
@@ -226,18 +229,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (b.part < 2) {
         const uint8_t* in1 = in0 + (DQK / 32) * kInBox;
         const float mu = row_mean_dot<DQK>(in0, in1, r);
-        const float2* rope_row = rope + pos;
-#pragma unroll 1
+#pragma unroll
         for (int gg = 0; gg < DQK / 32; ++gg) {
           float a[16], c[16];
-          dy_group<DQK>(in0, in1, r, mu, rstd, rope_row, p.max_pos, gg, a, c);
+          dy_group<DQK>(in0, in1, r, mu, rstd, cs, gg, a, c);
           if (!valid) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) a[j] = c[j] = 0.f;
           }
           if (QUANT) {
-            emit16(a, s_dy, rs_dy, r, gg * 16, out8);
-            emit16(c, s_dy, rs_dy, r, DQK / 2 + gg * 16, out8);
+            emit16(a, kq, r, gg * 16, out8);
+            emit16(c, kq, r, DQK / 2 + gg * 16, out8);
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fmaxf(fabsf(a[j]), fabsf(c[j])));
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
           }
           if (QUANT) {
-            emit16(v, s_dy, rs_dy, r, c0, out8);
+            emit16(v, kq, r, c0, out8);
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(v[j]));

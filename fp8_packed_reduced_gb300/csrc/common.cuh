@@ -252,29 +252,43 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
   return quant1(a, s) | (quant1(b, s) << 8) | (quant1(c, s) << 16) | (quant1(d, s) << 24);
 }
 
-// The same code as quant1(v, s), from a multiplication by rs = 1/s (rounded
-// to nearest).  q = v * rs is within 2^-22 (relative) of the IEEE quotient
-// fl(v/s), so the quotient lies inside [q (1 - 2^-20), q (1 + 2^-20)] (the
-// bracket's own rounding is 2^-24).  Rounding onto the E4M3 grid with
-// saturation is monotone, so when both ends of the bracket give the same code
-// that is the quotient's code; otherwise (q within 2^-20 of a rounding
-// boundary) the exact division decides.  For |q| below 2^-11 both ends and
-// the quotient give a signed zero of q's sign.
+// Exact codes from multiplications.  With rs = fl(1/s), lo = fl(rs (1 - 2^-20))
+// and hi = fl(rs (1 + 2^-20)) (a Bracket), fl(v lo) and fl(v hi) lie on either
+// side of the IEEE quotient fl(v/s): each product is within 3 * 2^-24 of
+// v/s (1 -+ 2^-20) and the quotient within 2^-24 of v/s.  Rounding onto the
+// E4M3 grid with saturation is monotone, so when both products give the same
+// code that is the quotient's code; otherwise (v/s within ~2^-20 of a
+// rounding boundary, rare) the exact division decides.  Products below the
+// smallest E4M3 step give a signed zero of v's sign on both sides, as the
+// quotient does; |v/s| <= 448 (1 + 2^-23) for the tensors quantised here, so
+// no product overflows.
+struct Bracket {
+  float s, lo, hi;
+};
+__device__ __forceinline__ Bracket make_bracket(float s) {
+  const float rs = __frcp_rn(s);
+  return Bracket{s, rs * 0.99999904632568359375f, rs * 1.00000095367431640625f};
+}
+
 // The rare exact path, kept out of line so the division is executed only when
 // a bracket straddles a rounding boundary (not predicated for every value).
-static __device__ __noinline__ uint32_t quant1_exact(float v, float s) { return quant1(v, s); }
-
-__device__ __forceinline__ uint32_t quant1_fast(float v, float s, float rs) {
-  const float q = v * rs;
-  const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
-      make_float2(q * 0.99999904632568359375f, q * 1.00000095367431640625f), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t lo = c & 0xFFu, hi = (c >> 8) & 0xFFu;
-  if (__builtin_expect(lo == hi, 1)) return lo;
-  return quant1_exact(v, s);
+static __device__ __noinline__ uint32_t quant2_exact(float a, float b, float s) {
+  return quant1(a, s) | (quant1(b, s) << 8);
 }
-__device__ __forceinline__ uint32_t quant4_fast(float a, float b, float c, float d, float s, float rs) {
-  return quant1_fast(a, s, rs) | (quant1_fast(b, s, rs) << 8) | (quant1_fast(c, s, rs) << 16) |
-         (quant1_fast(d, s, rs) << 24);
+
+// Two codes (a in the low byte).
+__device__ __forceinline__ uint32_t quant2_fast(float a, float b, const Bracket& k) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a * k.lo, b * k.lo), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a * k.hi, b * k.hi), __NV_SATFINITE, __NV_E4M3);
+  if (__builtin_expect(lo == hi, 1)) {
+    // __nv_cvt_float2_to_fp8x2 puts .x in the low byte
+    return lo;
+  }
+  return quant2_exact(a, b, k.s);
+}
+// Four codes packed little-endian (a in the lowest byte).
+__device__ __forceinline__ uint32_t quant4_fast(float a, float b, float c, float d, const Bracket& k) {
+  return quant2_fast(a, b, k) | (quant2_fast(c, d, k) << 16);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -175,6 +175,7 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
     int it = 0;
     for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x, ++it) {
       const int buf = it & 1;
+      epi.prepare(u);  // loads that do not depend on the accumulator
       if (!mbar_wait(&g.tfull[buf], (it >> 1) & 1, &g.abort_flag, st, kid)) break;
       tc_fence_after();
       epi.process(u, tmem_base + static_cast<uint32_t>(buf * 256) + (static_cast<uint32_t>(qw * 32) << 16));
@@ -284,6 +285,31 @@ struct FwdEpi {
   uint8_t* stage;
   int qw, sub, nsub, lane;
   float sxw;
+  // per unit, set by prepare(): tile decode, this thread's token and its
+  // cos/sin for every rotation pair (shared by the q/k heads of the tile)
+  int kind, head0, nh, t;
+  bool valid;
+  float2 cs[DQK / 2];
+
+  __device__ void prepare(int u) {
+    const int m = u / p.n_tiles;
+    sc.decode(u % p.n_tiles, kind, head0, nh);
+    t = m * kBM + qw * 32 + lane;
+    valid = t < p.T;
+    if (kind < 2) {
+      int pos = 0;
+      if (valid) {
+        pos = __ldg(p.pos + t);
+        if (pos < 0 || pos >= p.max_pos) {
+          record_error(st, QKVP_ERR_DEVICE_INPUT, KID_FWD_GEMM);
+          pos = 0;
+        }
+      }
+      const float2* rope = reinterpret_cast<const float2*>(p.rope) + pos;
+#pragma unroll
+      for (int i = 0; i < DQK / 2; ++i) cs[i] = __ldg(rope + static_cast<int64_t>(i) * p.max_pos);
+    }
+  }
 
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t* stage_) {
     qw = qw_;
@@ -306,22 +332,7 @@ struct FwdEpi {
 
   __device__ void process(int u, uint32_t tacc) {
     constexpr int HALF = DQK / 2;
-    const int m = u / p.n_tiles, j = u % p.n_tiles;
-    int kind, head0, nh;
-    sc.decode(j, kind, head0, nh);
-    const int row = qw * 32 + lane;
-    const int t = m * kBM + row;
-    const int ty = m * kBM + qw * 32;
-    const bool valid = t < p.T;
-    int pos = 0;
-    if (valid && kind < 2) {
-      pos = __ldg(p.pos + t);
-      if (pos < 0 || pos >= p.max_pos) {
-        record_error(st, QKVP_ERR_DEVICE_INPUT, KID_FWD_GEMM);
-        pos = 0;
-      }
-    }
-    const float2* rope = reinterpret_cast<const float2*>(p.rope);
+    const int ty = (u / p.n_tiles) * kBM + qw * 32;
     for (int hh = sub; hh < nh; hh += nsub) {  // this warp's heads of the unit
       const int h = head0 + hh;
       uint8_t* buf = acquire();
@@ -345,8 +356,8 @@ struct FwdEpi {
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
             const int c = g * 16 + i;
-            const float2 cs0 = __ldg(rope + static_cast<int64_t>(c) * p.max_pos + pos);
-            const float2 cs1 = __ldg(rope + static_cast<int64_t>(c + 1) * p.max_pos + pos);
+            const float2 cs0 = cs[c];
+            const float2 cs1 = cs[c + 1];
             const float a0 = v[c] * r, a1 = v[c + 1] * r;
             const float b0 = v[HALF + c] * r, b1 = v[HALF + c + 1] * r;
             lo[i / 2] = pack_bf16x2(a0 * cs0.x - b0 * cs0.y, a1 * cs1.x - b1 * cs1.y);
@@ -449,6 +460,7 @@ struct DxEpi {
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
   }
+  __device__ void prepare(int) {}
   __device__ void process(int u, uint32_t tacc) {
     const int m = u / p.n_tiles, j = u % p.n_tiles;
     const int ty = m * kBM + qw * 32;
@@ -532,6 +544,7 @@ struct DwEpi {
     lane = lane_;
   }
   __device__ void finish() {}
+  __device__ void prepare(int) {}
   __device__ void process(int u, uint32_t tacc) {
     // unit u owns partials[u][bn][128] (column-major tile): coalesced stores
     float* dst = p.partials + static_cast<int64_t>(u) * p.bn * kBM + qw * 32 + lane;

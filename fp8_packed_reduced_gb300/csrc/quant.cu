@@ -29,10 +29,12 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restri
   float m = 0.f;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < n16; i += 4 * stride) {  // four independent loads in flight
-    const uint4 a = __ldg(p + i), b = __ldg(p + i + stride), c = __ldg(p + i + 2 * stride),
-                d = __ldg(p + i + 3 * stride);
-    m = fmaxf(m, fmaxf(fmaxf(absmax_bf16x8(a), absmax_bf16x8(b)), fmaxf(absmax_bf16x8(c), absmax_bf16x8(d))));
+  for (; i + 7 * stride < n16; i += 8 * stride) {  // eight independent loads in flight
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __ldg(p + i + j * stride);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, absmax_bf16x8(v[j]));
   }
   for (; i < n16; i += stride) m = fmaxf(m, absmax_bf16x8(__ldg(p + i)));
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail)
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__
   const int n0 = (blockIdx.x / tiles_d) * 128, d0 = (blockIdx.x % tiles_d) * 128;
   const float amax = block_reduce_partials(partials + l * kBankAmaxBlocks, kBankAmaxBlocks, red);
   const float s = scale_from_amax(amax);
-  const float rs = __frcp_rn(s);
+  const Bracket k = make_bracket(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) a.w_scale[l] = s;
 
   const int r = threadIdx.x >> 1;          // tile row
@@ -105,8 +107,7 @@ __global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__
       uint32_t c[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        c[q] = quant4_fast(bf16_lo(w[2 * q]), bf16_hi(w[2 * q]), bf16_lo(w[2 * q + 1]), bf16_hi(w[2 * q + 1]), s,
-                           rs);
+        c[q] = quant4_fast(bf16_lo(w[2 * q]), bf16_hi(w[2 * q]), bf16_lo(w[2 * q + 1]), bf16_hi(w[2 * q + 1]), k);
       *reinterpret_cast<uint4*>(W8 + static_cast<int64_t>(n) * a.D + d0 + ch + j * 8) =
           make_uint4(c[0], c[1], c[2], c[3]);
 #pragma unroll
@@ -150,12 +151,12 @@ cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStre
 // x (a few KB from L2), then converts 16 values per thread per step: two
 // 16-byte loads, one 16-byte store.  T * D is a multiple of 16 (D % 128 == 0).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 quant16(uint4 u0, uint4 u1, float s, float rs) {
+__device__ __forceinline__ uint4 quant16(uint4 u0, uint4 u1, const Bracket& k) {
   const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
   uint32_t q[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    q[j] = quant4_fast(bf16_lo(w[2 * j]), bf16_hi(w[2 * j]), bf16_lo(w[2 * j + 1]), bf16_hi(w[2 * j + 1]), s, rs);
+    q[j] = quant4_fast(bf16_lo(w[2 * j]), bf16_hi(w[2 * j]), bf16_lo(w[2 * j + 1]), bf16_hi(w[2 * j + 1]), k);
   return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(256) x_quant_kernel(const uint16_t* __restrict
                                                       float* x_scale) {
   __shared__ float red[32];
   const float s = scale_from_amax(block_reduce_partials(partials, nparts, red));
-  const float rs = __frcp_rn(s);
+  const Bracket k = make_bracket(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) *x_scale = s;
   const uint4* src = reinterpret_cast<const uint4*>(x);
   uint4* dst = reinterpret_cast<uint4*>(x8);
@@ -173,10 +174,10 @@ __global__ void __launch_bounds__(256) x_quant_kernel(const uint16_t* __restrict
   for (; i + stride < n16; i += 2 * stride) {  // two independent groups in flight
     const uint4 a0 = __ldg(src + 2 * i), a1 = __ldg(src + 2 * i + 1);
     const uint4 b0 = __ldg(src + 2 * (i + stride)), b1 = __ldg(src + 2 * (i + stride) + 1);
-    dst[i] = quant16(a0, a1, s, rs);
-    dst[i + stride] = quant16(b0, b1, s, rs);
+    dst[i] = quant16(a0, a1, k);
+    dst[i + stride] = quant16(b0, b1, k);
   }
-  for (; i < n16; i += stride) dst[i] = quant16(__ldg(src + 2 * i), __ldg(src + 2 * i + 1), s, rs);
+  for (; i < n16; i += stride) dst[i] = quant16(__ldg(src + 2 * i), __ldg(src + 2 * i + 1), k);
 }
 
 cudaError_t launch_x_quant(const uint16_t* x, int64_t n, uint8_t* x8, const float* partials, int nparts,

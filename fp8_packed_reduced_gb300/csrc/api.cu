@@ -363,7 +363,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   ok = ok && map3d(&m.dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&m.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, dvw, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map2d(&m.dy8, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && map2d(&m.dy8, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_32B);
   // dY8 [T, N] read as 128 x 128 tiles: K-major A of the dX GEMM, MN-major A of the dW GEMM
   CUtensorMap tm_dy, tm_w8t, tm_dx, tm_x8;
   ok = ok && map2d(&tm_dy, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);

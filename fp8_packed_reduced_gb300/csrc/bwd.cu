@@ -14,12 +14,17 @@
 //
 // Work unit: 128 tokens x one head x one part (q, k or v).  Persistent CTA
 // per SM, warp-specialised:
-//   warp 0      TMA producer: the unit's input boxes ([128 tokens x 32 cols],
-//               64-byte swizzle) into a ring of kBwdStages stages
-//   warps 1-8   two consumer groups of four warps; group g takes every other
-//               unit of the CTA; one token row per thread (conflict-free reads
-//               of the swizzled boxes); pass 2 stages the codes of its unit and
-//               stores them by TMA while the other group computes
+//   warp 0       TMA producer: the unit's input boxes ([128 tokens x 32 cols],
+//                64-byte swizzle) into a ring of kBwdStages stages
+//   warps 1-16   two consumer groups of eight warps; group g takes every
+//                other unit of the CTA.  Two threads per token row: thread
+//                half h owns the 8-column blocks (c / 8) % 2 == h of the row,
+//                which keeps each rotation pair (i, i + d/2) in one thread;
+//                the row's mean(g_out * o) is one shuffle between the two.
+//                Pass 2 stages the codes of its unit (32-byte swizzle) and
+//                stores them by TMA while the other group computes.
+// Within a warp, lanes map to rows so that the 16-byte reads of a quarter
+// warp hit eight distinct 16-byte bank groups of the swizzled boxes.
 #include "kernels.cuh"
 
 namespace qkvp {
@@ -27,7 +32,8 @@ namespace qkvp {
 constexpr int kInBox = 8192;        // 128 rows x 32 bf16
 constexpr int kOutBox = 4096;       // 128 rows x 32 codes
 constexpr int kBwdStages = 3;
-constexpr int kBwdThreads = 32 * 9;
+constexpr int kGroupThreads = 256;
+constexpr int kBwdThreads = 32 + 2 * kGroupThreads;
 
 __host__ __device__ constexpr int bwd_stage_bytes(int d_qk) {
   return (2 * d_qk > 128 ? 2 * d_qk : 128) / 32 * kInBox;   // max(dq+q, dv) boxes
@@ -49,64 +55,49 @@ __device__ __forceinline__ BwdUnit bwd_decode(const BwdParams& p, int u) {
   return b;
 }
 
-// 16 consecutive bf16 values of row r starting at column c0 (c0 % 16 == 0)
-// of a group of 32-column boxes with 64-byte swizzling.
-__device__ __forceinline__ void load16(const uint8_t* boxes, int r, int c0, float (&v)[16]) {
-  const uint8_t* box = boxes + (c0 >> 5) * kInBox + r * 64;
-  const int cc = (c0 & 31) >> 3;
-  const uint4 x0 = *reinterpret_cast<const uint4*>(box + ((cc ^ ((r >> 1) & 3)) << 4));
-  const uint4 x1 = *reinterpret_cast<const uint4*>(box + (((cc + 1) ^ ((r >> 1) & 3)) << 4));
-  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+// Row of the unit and column half owned by a consumer thread (index 0..255
+// inside its group).  Lanes 8k..8k+7 of a warp cover rows {b, b+1, b+4, b+5}
+// of the warp's 16 rows, both halves each.
+__device__ __forceinline__ void row_and_half(int gt, int& r, int& h) {
+  const int warp = gt >> 5, lane = gt & 31;
+  const int j = (lane >> 1) & 3, q = lane >> 3;
+  h = lane & 1;
+  r = warp * 16 + (q & 1) * 2 + (q >> 1) * 8 + (j & 1) + (j >> 1) * 4;
+}
+
+// The 16-byte chunk holding columns [c, c + 8) (c % 8 == 0) of row r of a
+// group of 32-column boxes with 64-byte swizzling.
+__device__ __forceinline__ uint4 load8(const uint8_t* boxes, int r, int c) {
+  const int cc = (c & 31) >> 3;
+  return *reinterpret_cast<const uint4*>(boxes + (c >> 5) * kInBox + r * 64 + ((cc ^ ((r >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ void unpack8(uint4 x, float (&v)[8]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     v[2 * i] = bf16_lo(w[i]);
     v[2 * i + 1] = bf16_hi(w[i]);
   }
 }
 
-// mean(g_out * o) over row r of a q/k unit.
-template <int DQK>
-__device__ __forceinline__ float row_mean_dot(const uint8_t* in0, const uint8_t* in1, int r) {
-  float dot = 0.f;
-#pragma unroll 2
-  for (int c0 = 0; c0 < DQK; c0 += 16) {
-    float g[16], o[16];
-    load16(in0, r, c0, g);
-    load16(in1, r, c0, o);
+__device__ __forceinline__ float dot8(uint4 a, uint4 b) {
+  float x[8], y[8];
+  unpack8(a, x);
+  unpack8(b, y);
+  float d = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) dot = fmaf(g[j], o[j], dot);
-  }
-  return __fdiv_rn(dot, static_cast<float>(DQK));
+  for (int i = 0; i < 8; ++i) d = fmaf(x[i], y[i], d);
+  return d;
 }
 
-// dY of row r of a q or k unit for 16 rotation pairs: columns [16g, 16g+16)
-// into a[] and [HALF+16g, HALF+16g+16) into b[].
-template <int DQK>
-__device__ __forceinline__ void dy_group(const uint8_t* in0, const uint8_t* in1, int r, float mu, float rstd,
-                                         const float2 (&cs)[DQK / 2], int g, float (&a)[16], float (&b)[16]) {
-  constexpr int HALF = DQK / 2;
-  float ga[16], gb[16], oa[16], ob[16];
-  load16(in0, r, g * 16, ga);
-  load16(in0, r, HALF + g * 16, gb);
-  load16(in1, r, g * 16, oa);
-  load16(in1, r, HALF + g * 16, ob);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float ua = ga[j] - mu * oa[j];
-    const float ub = gb[j] - mu * ob[j];
-    const float2 c = cs[g * 16 + j];
-    a[j] = rstd * (ua * c.x + ub * c.y);
-    b[j] = rstd * (ub * c.x - ua * c.y);
-  }
-}
-
-// Codes of 16 consecutive columns [c0, c0+16) of row r into the token-major
-// staging boxes [128 rows][32 codes].
-__device__ __forceinline__ void emit16(const float (&v)[16], const Bracket& k, int r, int c0, uint8_t* out8) {
-  uint32_t w[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) w[q] = quant4_fast(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], k);
-  *reinterpret_cast<uint4*>(out8 + (c0 >> 5) * kOutBox + r * 32 + (c0 & 31)) = make_uint4(w[0], w[1], w[2], w[3]);
+// Eight codes of columns [c, c + 8) (c % 8 == 0) of row r into the
+// token-major staging boxes [128 rows][32 codes] with 32-byte swizzling
+// (the 16-byte half of a row is XORed with bit 2 of the row).
+__device__ __forceinline__ void emit8(const float (&v)[8], const Bracket& k, int r, int c, uint8_t* out8) {
+  const uint2 w = make_uint2(quant4_fast(v[0], v[1], v[2], v[3], k), quant4_fast(v[4], v[5], v[6], v[7], k));
+  const int cl = c & 31;
+  *reinterpret_cast<uint2*>(out8 + (c >> 5) * kOutBox + r * 32 + (((cl >> 4) ^ ((r >> 2) & 1)) << 4) + (cl & 15)) = w;
 }
 
 // Per-row saved state of a q/k unit: rstd and position (checked).
@@ -124,20 +115,20 @@ __device__ __forceinline__ void row_state(const BwdParams& p, const BwdUnit& b, 
 }
 
 __device__ __forceinline__ void group_sync(int g) {
-  asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(kGroupThreads) : "memory");
 }
 
-// AND of `v` over the 128 threads of consumer group g (all of them call it),
-// so that the group leaves its loop together.
+// AND of `v` over the threads of consumer group g (all of them call it), so
+// that the group leaves its loop together.
 __device__ __forceinline__ bool group_all(int g, bool v) {
   uint32_t out;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, %2, 128, q;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(out)
-      : "r"(static_cast<uint32_t>(v)), "r"(1 + g)
+      : "r"(static_cast<uint32_t>(v)), "r"(1 + g), "n"(kGroupThreads)
       : "memory");
   return out != 0;
 }
@@ -148,6 +139,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_epi_kernel(const __grid_constant__ BwdMaps m, const __grid_constant__ BwdParams p, DevStatus st) {
   constexpr int kid = QUANT ? KID_BWD_QUANT : KID_BWD_AMAX;
   constexpr int kStage = bwd_stage_bytes(DQK);
+  constexpr int HALF = DQK / 2;      // rotation pairs per row
+  constexpr int NG = HALF / 16;      // 16-pair groups; this thread owns 8 pairs of each
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[kBwdStages], empty[kBwdStages];
@@ -159,7 +152,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     abort_flag = 0;
     for (int s = 0; s < kBwdStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 128);
+      mbar_init(&empty[s], kGroupThreads);
     }
     fence_mbar_init();
   }
@@ -199,8 +192,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (used & (1u << s)) mbar_wait(&full[s], (last_par >> s) & 1, nullptr, st, kid);
     }
   } else {
-    const int g = (warp - 1) >> 2;                 // consumer group
-    const int r = ((warp - 1) & 3) * 32 + lane;    // token row of the unit
+    const int g = (warp - 1) >> 3;                            // consumer group
+    const int gt = threadIdx.x - 32 - g * kGroupThreads;      // thread index inside the group
+    int r, hf;
+    row_and_half(gt, r, hf);
     uint8_t* out8 = smem + kBwdStages * kStage + g * 4 * kOutBox;
     const float2* rope = reinterpret_cast<const float2*>(p.rope);
     int it = g;
@@ -211,16 +206,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool valid = t < p.T;
       float rstd;
       int pos;
-      float2 cs[DQK / 2];  // this row's cos/sin, loaded before the inputs arrive
-      if (b.part < 2) {
-        row_state(p, b, t, rstd, pos, st, kid);
-        const float2* rope_row = rope + pos;
-#pragma unroll
-        for (int i = 0; i < DQK / 2; ++i) cs[i] = __ldg(rope_row + static_cast<int64_t>(i) * p.max_pos);
-      }
+      if (b.part < 2) row_state(p, b, t, rstd, pos, st, kid);
       if (QUANT) {
         // the previous unit's stores have read this group's staging tiles
-        if (r == 0) bulk_wait_read<0>();
+        if (gt == 0) bulk_wait_read<0>();
         group_sync(g);
       }
       if (!group_all(g, mbar_wait(&full[s], (it / kBwdStages) & 1, &abort_flag, st, kid))) break;
@@ -228,53 +217,75 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int nbox;
       if (b.part < 2) {
         const uint8_t* in1 = in0 + (DQK / 32) * kInBox;
-        const float mu = row_mean_dot<DQK>(in0, in1, r);
+        const float2* rope_row = rope + pos;
+        float dot = 0.f;
 #pragma unroll
-        for (int gg = 0; gg < DQK / 32; ++gg) {
-          float a[16], c[16];
-          dy_group<DQK>(in0, in1, r, mu, rstd, cs, gg, a, c);
-          if (!valid) {
+        for (int gg = 0; gg < NG; ++gg) {
+          const int c = 16 * gg + 8 * hf;
+          dot += dot8(load8(in0, r, c), load8(in1, r, c)) + dot8(load8(in0, r, HALF + c), load8(in1, r, HALF + c));
+        }
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);   // the row's other half
+        const float mu = __fdiv_rn(dot, static_cast<float>(DQK));
 #pragma unroll
-            for (int j = 0; j < 16; ++j) a[j] = c[j] = 0.f;
+        for (int gg = 0; gg < NG; ++gg) {
+          const int c = 16 * gg + 8 * hf;
+          float2 k2[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) k2[j] = __ldg(rope_row + static_cast<int64_t>(c + j) * p.max_pos);
+          float ga[8], gb[8], oa[8], ob[8], a[8], c2[8];
+          unpack8(load8(in0, r, c), ga);
+          unpack8(load8(in0, r, HALF + c), gb);
+          unpack8(load8(in1, r, c), oa);
+          unpack8(load8(in1, r, HALF + c), ob);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float ua = ga[j] - mu * oa[j];
+            const float ub = gb[j] - mu * ob[j];
+            a[j] = valid ? rstd * (ua * k2[j].x + ub * k2[j].y) : 0.f;
+            c2[j] = valid ? rstd * (ub * k2[j].x - ua * k2[j].y) : 0.f;
           }
           if (QUANT) {
-            emit16(a, kq, r, gg * 16, out8);
-            emit16(c, kq, r, DQK / 2 + gg * 16, out8);
+            emit8(a, kq, r, c, out8);
+            emit8(c2, kq, r, HALF + c, out8);
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fmaxf(fabsf(a[j]), fabsf(c[j])));
+            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fmaxf(fabsf(a[j]), fabsf(c2[j])));
           }
         }
+        mbar_arrive(&empty[s]);  // this thread is done with the stage
         nbox = DQK / 32;
       } else {
-#pragma unroll 2
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-          float v[16];
-          load16(in0, r, c0, v);
+        uint4 x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = load8(in0, r, 16 * q + 8 * hf);
+        mbar_arrive(&empty[s]);  // inputs now in registers
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float v[8];
+          unpack8(x[q], v);
           if (!valid) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            for (int j = 0; j < 8; ++j) v[j] = 0.f;
           }
           if (QUANT) {
-            emit16(v, kq, r, c0, out8);
+            emit8(v, kq, r, 16 * q + 8 * hf, out8);
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(v[j]));
+            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(v[j]));
           }
         }
         nbox = 4;
       }
-      mbar_arrive(&empty[s]);  // this thread is done with the stage
       if (QUANT) {
         fence_async_smem();
         group_sync(g);
-        if (r == 0) {
+        if (gt == 0) {
           for (int j = 0; j < nbox; ++j) tma_store_2d(&m.dy8, out8 + j * kOutBox, b.col0 + 32 * j, b.t0);
           bulk_commit();
         }
       }
     }
-    if (QUANT && r == 0) bulk_wait_all<0>();
+    if (QUANT && gt == 0) bulk_wait_all<0>();
   }
   if (!QUANT) {
     mx = block_max(mx, red);

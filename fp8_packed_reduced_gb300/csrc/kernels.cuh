@@ -94,7 +94,7 @@ struct BwdParams {
 };
 struct BwdMaps {
   CUtensorMap dq, q, dk, k, dv;   // loads, 3-D [H][T][d], box {32, 128, 1}, 64-byte swizzle
-  CUtensorMap dy8;                // store: [T][N] codes, box {32, 128}
+  CUtensorMap dy8;                // store: [T][N] codes, box {32, 128}, 32-byte swizzle
 };
 cudaError_t launch_bwd_amax(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s);
 cudaError_t launch_bwd_quant(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s);

@@ -31,15 +31,16 @@ namespace qkvp {
 
 constexpr int kInBox = 8192;        // 128 rows x 32 bf16
 constexpr int kOutBox = 4096;       // 128 rows x 32 codes
-constexpr int kBwdStages = 3;
 constexpr int kGroupThreads = 256;
 constexpr int kBwdThreads = 32 + 2 * kGroupThreads;
 
 __host__ __device__ constexpr int bwd_stage_bytes(int d_qk) {
   return (2 * d_qk > 128 ? 2 * d_qk : 128) / 32 * kInBox;   // max(dq+q, dv) boxes
 }
+// As many stages as fit beside the code staging: 4 at d_qk <= 96, 3 at 128.
+__host__ __device__ constexpr int bwd_stages(int d_qk) { return d_qk <= 96 ? 4 : 3; }
 __host__ __device__ constexpr int bwd_smem_bytes(int d_qk, bool quant) {
-  return 1024 + kBwdStages * bwd_stage_bytes(d_qk) + (quant ? 2 * 4 * kOutBox : 0);
+  return 1024 + bwd_stages(d_qk) * bwd_stage_bytes(d_qk) + (quant ? 2 * 4 * kOutBox : 0);
 }
 
 struct BwdUnit {
@@ -139,11 +140,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_epi_kernel(const __grid_constant__ BwdMaps m, const __grid_constant__ BwdParams p, DevStatus st) {
   constexpr int kid = QUANT ? KID_BWD_QUANT : KID_BWD_AMAX;
   constexpr int kStage = bwd_stage_bytes(DQK);
+  constexpr int kBwdStages = bwd_stages(DQK);
   constexpr int HALF = DQK / 2;      // rotation pairs per row
   constexpr int NG = HALF / 16;      // 16-pair groups; this thread owns 8 pairs of each
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kBwdStages], empty[kBwdStages];
+  __shared__ __align__(8) uint64_t full[4], empty[4];
   __shared__ float red[32];
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

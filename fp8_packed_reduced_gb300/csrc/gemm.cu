@@ -30,7 +30,6 @@ constexpr int kBStage = 256 * kBK;         // 32 KB (largest B tile)
 // Threads of a GEMM CTA with EW epilogue warps (4 or 8).
 __host__ __device__ constexpr int gemm_threads(int ew) { return 64 + 32 * ew; }
 constexpr int kTmemCols = 512;             // 2 accumulators x 256 fp32 columns
-constexpr int kEpiWarpBytes = 8192;        // staging per epilogue warp: 4 boxes of 32 rows x 64 B
 constexpr int kMaxStages = 6;
 
 struct Unit {
@@ -49,8 +48,10 @@ struct GemmSmem {
   int abort_flag;
 };
 
-__host__ __device__ constexpr int gemm_smem_bytes(int stages, int ew, bool epi_staging) {
-  return 1024 + stages * (kAStage + kBStage) + (epi_staging ? ew * kEpiWarpBytes : 0);
+// Dynamic shared memory: alignment slack, the stage ring, and `epb` bytes of
+// output staging per epilogue warp (boxes of 32 rows x 64 B).
+__host__ __device__ constexpr int gemm_smem_bytes(int stages, int ew, int epb) {
+  return 1024 + stages * (kAStage + kBStage) + ew * epb;
 }
 
 // ---------------------------------------------------------------------------
@@ -129,7 +130,7 @@ __device__ void mma_role(const Sched& sc, uint8_t* sA, uint8_t* sB, GemmSmem& g,
 // ---------------------------------------------------------------------------
 // Common body
 // ---------------------------------------------------------------------------
-template <int EW, class Sched, class Epi>
+template <int EW, int EPB, class Sched, class Epi>
 __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUtensorMap* tmA,
                                           const CUtensorMap* tmB, int stages, const DevStatus& st, int kid) {
   extern __shared__ uint8_t smem_raw[];
@@ -171,7 +172,7 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
   } else {
     const int qw = warp & 3;          // TMEM lane quarter this warp may access
     const int sub = (warp - 2) >> 2;  // which share of the unit's heads / columns
-    epi.begin(qw, sub, EW / 4, lane, sE + (warp - 2) * kEpiWarpBytes);
+    epi.begin(qw, sub, EW / 4, lane, sE + (warp - 2) * EPB);
     int it = 0;
     for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x, ++it) {
       const int buf = it & 1;
@@ -282,8 +283,8 @@ struct FwdEpi {
   const CUtensorMap* tk;
   const CUtensorMap* tv;
   const DevStatus& st;
-  uint8_t* stage;
-  int qw, sub, nsub, lane;
+  uint8_t* stage;   // two 8 KB halves: a head's boxes go to one while the other's store drains
+  int qw, sub, nsub, lane, half;
   float sxw;
   // per unit, set by prepare(): tile decode, this thread's token and its
   // cos/sin for every rotation pair (shared by the q/k heads of the tile)
@@ -317,17 +318,20 @@ struct FwdEpi {
     nsub = nsub_;
     lane = lane_;
     stage = stage_;
+    half = 0;
     sxw = (*p.x_scale) * (*p.w_scale);
   }
   __device__ void finish() {
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
   }
-  // wait until the stores that last read this warp's staging boxes are done
+  // the half used two heads ago: wait until its store has read it
   __device__ uint8_t* acquire() {
-    if (lane == 0) bulk_wait_read<0>();
+    if (lane == 0) bulk_wait_read<1>();
     __syncwarp();
-    return stage;
+    uint8_t* b = stage + half * 8192;
+    half ^= 1;
+    return b;
   }
 
   __device__ void process(int u, uint32_t tacc) {
@@ -403,7 +407,9 @@ struct FwdEpi {
   }
 };
 
+// Epilogue warps and per-warp staging bytes of each GEMM.
 constexpr int kFwdEW = 4, kDxEW = 4, kDwEW = 8;
+constexpr int kFwdEPB = 16384, kDxEPB = 8192;
 
 template <int DQK>
 __global__ void __launch_bounds__(gemm_threads(kFwdEW), 1)
@@ -414,7 +420,7 @@ __global__ void __launch_bounds__(gemm_threads(kFwdEW), 1)
                     int stages) {
   FwdSched sc{p, &tmBv};
   FwdEpi<DQK> epi{p, sc, &tq, &tk, &tv, st};
-  gemm_body<kFwdEW>(sc, epi, &tmA, &tmB, stages, st, KID_FWD_GEMM);
+  gemm_body<kFwdEW, kFwdEPB>(sc, epi, &tmA, &tmB, stages, st, KID_FWD_GEMM);
 }
 
 // ---------------------------------------------------------------------------
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(gemm_threads(kDxEW), 1)
                    int stages) {
   DxSched sc{p};
   DxEpi epi{p, &tdx};
-  gemm_body<kDxEW>(sc, epi, &tmA, &tmB, stages, st, KID_DX_GEMM);
+  gemm_body<kDxEW, kDxEPB>(sc, epi, &tmA, &tmB, stages, st, KID_DX_GEMM);
 }
 
 // ---------------------------------------------------------------------------
@@ -565,7 +571,7 @@ __global__ void __launch_bounds__(gemm_threads(kDwEW), 1)
                    const __grid_constant__ DwParams p, DevStatus st, int stages) {
   DwSched sc{p};
   DwEpi epi{p};
-  gemm_body<kDwEW>(sc, epi, &tmA, &tmB, stages, st, KID_DW_GEMM);
+  gemm_body<kDwEW, 0>(sc, epi, &tmA, &tmB, stages, st, KID_DW_GEMM);
 }
 
 // dW[n][d] = bf16(s_dy * s_x * sum over splits, in split order, of the
@@ -599,7 +605,7 @@ __global__ void __launch_bounds__(256) dw_reduce_kernel(const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
-constexpr int kFwdStages = 4, kDxStages = 4, kDwStages = 4;
+constexpr int kFwdStages = 3, kDxStages = 4, kDwStages = 4;
 
 template <class K>
 static cudaError_t set_smem_once(K kernel, int bytes, bool (&done)[64]) {
@@ -618,7 +624,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, 
                                 const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
                                 DevStatus st, cudaStream_t s) {
   static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kFwdStages, kFwdEW, true);
+  const int smem = gemm_smem_bytes(kFwdStages, kFwdEW, kFwdEPB);
   cudaError_t e = set_smem_once(fwd_gemm_kernel<DQK>, smem, done);
   if (e != cudaSuccess) return e;
   fwd_gemm_kernel<DQK><<<grid, gemm_threads(kFwdEW), smem, s>>>(tmA, tmB, tmBv, tq, tk, tv, p, st, kFwdStages);
@@ -639,7 +645,7 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
                            const DxParams& p, int grid, DevStatus st, cudaStream_t s) {
   static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kDxStages, kDxEW, true);
+  const int smem = gemm_smem_bytes(kDxStages, kDxEW, kDxEPB);
   cudaError_t e = set_smem_once(dx_gemm_kernel, smem, done);
   if (e != cudaSuccess) return e;
   dx_gemm_kernel<<<grid, gemm_threads(kDxEW), smem, s>>>(tmA, tmB, tdx, p, st, kDxStages);
@@ -649,7 +655,7 @@ cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int grid,
                            DevStatus st, cudaStream_t s) {
   static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kDwStages, kDwEW, false);
+  const int smem = gemm_smem_bytes(kDwStages, kDwEW, 0);
   cudaError_t e = set_smem_once(dw_gemm_kernel, smem, done);
   if (e != cudaSuccess) return e;
   dw_gemm_kernel<<<grid, gemm_threads(kDwEW), smem, s>>>(tmA, tmB, p, st, kDwStages);

@@ -136,9 +136,16 @@ struct TimingHook {
 } g_timing;
 
 // Recorded as an external event node when the stream is being captured into
-// a CUDA graph, so the graph's launches record it too.
+// a CUDA graph (so the graph's launches record it too), plainly otherwise.
 void mark(cudaStream_t s) {
-  if (g_timing.next < g_timing.n) cudaEventRecordWithFlags(g_timing.ev[g_timing.next++], s, cudaEventRecordExternal);
+  if (g_timing.next >= g_timing.n) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  cudaEvent_t ev = g_timing.ev[g_timing.next++];
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
 }
 
 #define QKVP_TRY_CUDA(expr)                          \

@@ -283,33 +283,29 @@ struct FwdEpi {
   const CUtensorMap* tk;
   const CUtensorMap* tv;
   const DevStatus& st;
-  uint8_t* stage;   // two 8 KB halves: a head's boxes go to one while the other's store drains
-  int qw, sub, nsub, lane, half;
+  uint8_t* stage;   // 8 KB: one head's boxes
+  int qw, sub, nsub, lane;
   float sxw;
-  // per unit, set by prepare(): tile decode, this thread's token and its
-  // cos/sin for every rotation pair (shared by the q/k heads of the tile)
+  // per unit, set by prepare() before the accumulator is ready: tile decode,
+  // this thread's token and its row of the RoPE table
   int kind, head0, nh, t;
   bool valid;
-  float2 cs[DQK / 2];
+  const float2* rope_row;
 
   __device__ void prepare(int u) {
     const int m = u / p.n_tiles;
     sc.decode(u % p.n_tiles, kind, head0, nh);
     t = m * kBM + qw * 32 + lane;
     valid = t < p.T;
-    if (kind < 2) {
-      int pos = 0;
-      if (valid) {
-        pos = __ldg(p.pos + t);
-        if (pos < 0 || pos >= p.max_pos) {
-          record_error(st, QKVP_ERR_DEVICE_INPUT, KID_FWD_GEMM);
-          pos = 0;
-        }
+    int pos = 0;
+    if (kind < 2 && valid) {
+      pos = __ldg(p.pos + t);
+      if (pos < 0 || pos >= p.max_pos) {
+        record_error(st, QKVP_ERR_DEVICE_INPUT, KID_FWD_GEMM);
+        pos = 0;
       }
-      const float2* rope = reinterpret_cast<const float2*>(p.rope) + pos;
-#pragma unroll
-      for (int i = 0; i < DQK / 2; ++i) cs[i] = __ldg(rope + static_cast<int64_t>(i) * p.max_pos);
     }
+    rope_row = reinterpret_cast<const float2*>(p.rope) + pos;
   }
 
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t* stage_) {
@@ -318,20 +314,17 @@ struct FwdEpi {
     nsub = nsub_;
     lane = lane_;
     stage = stage_;
-    half = 0;
     sxw = (*p.x_scale) * (*p.w_scale);
   }
   __device__ void finish() {
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
   }
-  // the half used two heads ago: wait until its store has read it
+  // wait until the previous head's store has read the staging boxes
   __device__ uint8_t* acquire() {
-    if (lane == 0) bulk_wait_read<1>();
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
-    uint8_t* b = stage + half * 8192;
-    half ^= 1;
-    return b;
+    return stage;
   }
 
   __device__ void process(int u, uint32_t tacc) {
@@ -341,31 +334,38 @@ struct FwdEpi {
       const int h = head0 + hh;
       uint8_t* buf = acquire();
       if (kind < 2) {
-        uint32_t raw[DQK];
-#pragma unroll
-        for (int c = 0; c < DQK / 16; ++c) tmem_ld16(tacc + hh * DQK + 16 * c, raw + 16 * c);
-        tmem_ld_wait();
-        float v[DQK];
+        // pass 1: sum of squares of the raw accumulators (scaled once below)
         float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < DQK; ++i) {
-          v[i] = __uint_as_float(raw[i]) * sxw;
-          ss = fmaf(v[i], v[i], ss);
+        for (int c = 0; c < DQK / 32; ++c) {
+          uint32_t raw[32];
+          tmem_ld16(tacc + hh * DQK + 32 * c, raw);
+          tmem_ld16(tacc + hh * DQK + 32 * c + 16, raw + 16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ss = fmaf(__uint_as_float(raw[i]), __uint_as_float(raw[i]), ss);
         }
+        ss *= sxw * sxw;
         const float r = 1.0f / sqrtf(__fdiv_rn(ss, static_cast<float>(DQK)) + p.eps);
         if (valid) p.rstd[(static_cast<int64_t>(kind) * p.H + h) * p.T + t] = r;
+        const float f = sxw * r;   // accumulator -> normalised value
+        // pass 2: rotate 16 pairs at a time, columns [16g, 16g+16) and [HALF+16g, HALF+16g+16)
 #pragma unroll
         for (int g = 0; g < HALF / 16; ++g) {
+          float2 cs[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) cs[i] = __ldg(rope_row + static_cast<int64_t>(g * 16 + i) * p.max_pos);
+          uint32_t ra[16], rb[16];
+          tmem_ld16(tacc + hh * DQK + g * 16, ra);
+          tmem_ld16(tacc + hh * DQK + HALF + g * 16, rb);
+          tmem_ld_wait();
           uint32_t lo[8], hi[8];
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
-            const int c = g * 16 + i;
-            const float2 cs0 = cs[c];
-            const float2 cs1 = cs[c + 1];
-            const float a0 = v[c] * r, a1 = v[c + 1] * r;
-            const float b0 = v[HALF + c] * r, b1 = v[HALF + c + 1] * r;
-            lo[i / 2] = pack_bf16x2(a0 * cs0.x - b0 * cs0.y, a1 * cs1.x - b1 * cs1.y);
-            hi[i / 2] = pack_bf16x2(b0 * cs0.x + a0 * cs0.y, b1 * cs1.x + a1 * cs1.y);
+            const float a0 = __uint_as_float(ra[i]) * f, a1 = __uint_as_float(ra[i + 1]) * f;
+            const float b0 = __uint_as_float(rb[i]) * f, b1 = __uint_as_float(rb[i + 1]) * f;
+            lo[i / 2] = pack_bf16x2(a0 * cs[i].x - b0 * cs[i].y, a1 * cs[i + 1].x - b1 * cs[i + 1].y);
+            hi[i / 2] = pack_bf16x2(b0 * cs[i].x + a0 * cs[i].y, b1 * cs[i + 1].x + a1 * cs[i + 1].y);
           }
           stage16(buf, lane, g * 16, lo);
           stage16(buf, lane, HALF + g * 16, hi);
@@ -408,8 +408,8 @@ struct FwdEpi {
 };
 
 // Epilogue warps and per-warp staging bytes of each GEMM.
-constexpr int kFwdEW = 4, kDxEW = 4, kDwEW = 8;
-constexpr int kFwdEPB = 16384, kDxEPB = 8192;
+constexpr int kFwdEW = 8, kDxEW = 4, kDwEW = 8;
+constexpr int kFwdEPB = 8192, kDxEPB = 8192;
 
 template <int DQK>
 __global__ void __launch_bounds__(gemm_threads(kFwdEW), 1)
@@ -575,31 +575,34 @@ __global__ void __launch_bounds__(gemm_threads(kDwEW), 1)
 }
 
 // dW[n][d] = bf16(s_dy * s_x * sum over splits, in split order, of the
-// partials).  grid: (m_tiles * n_tiles, bn / 32), 256 threads: thread =
-// (row in tile, 16-column half).
-__global__ void __launch_bounds__(256) dw_reduce_kernel(const __grid_constant__ DwParams p, const float* dy_scale,
+// partials).  One thread per (row, 4 columns): all of its splits' loads are
+// issued before the first add.  grid: (m_tiles * n_tiles, bn / 4), 128 threads.
+constexpr int kMaxReduceSplits = 16;
+__global__ void __launch_bounds__(128) dw_reduce_kernel(const __grid_constant__ DwParams p, const float* dy_scale,
                                                         const float* x_scale, uint16_t* dW) {
-  const int tile = blockIdx.x, c0 = blockIdx.y * 32 + (threadIdx.x >> 7) * 16;
-  const int row = threadIdx.x & 127;
+  const int tile = blockIdx.x, c0 = blockIdx.y * 4;
+  const int row = threadIdx.x;
   const int mn = p.m_tiles * p.n_tiles;
-  float acc[16];
+  float v[kMaxReduceSplits][4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  for (int s = 0; s < p.splits; ++s) {
-    const float* src = p.partials + (static_cast<int64_t>(s * mn + tile) * p.bn + c0) * kBM + row;
+  for (int s = 0; s < kMaxReduceSplits; ++s)
+    if (s < p.splits) {
+      const float* src = p.partials + (static_cast<int64_t>(s * mn + tile) * p.bn + c0) * kBM + row;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] += __ldcs(src + i * kBM);
-  }
+      for (int i = 0; i < 4; ++i) v[s][i] = __ldcs(src + i * kBM);
+    }
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < kMaxReduceSplits; ++s)
+    if (s < p.splits)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += v[s][i];
   const int n = (tile / p.n_tiles) * kBM + row;
   if (n >= p.N) return;
   const int d = (tile % p.n_tiles) * p.bn + c0;
   const float sc = (*dy_scale) * (*x_scale);
-  uint32_t w[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(acc[2 * i] * sc, acc[2 * i + 1] * sc);
-  uint4* out = reinterpret_cast<uint4*>(dW + static_cast<int64_t>(n) * p.D + d);
-  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  *reinterpret_cast<uint2*>(dW + static_cast<int64_t>(n) * p.D + d) =
+      make_uint2(pack_bf16x2(acc[0] * sc, acc[1] * sc), pack_bf16x2(acc[2] * sc, acc[3] * sc));
 }
 
 // ---------------------------------------------------------------------------
@@ -664,7 +667,8 @@ cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 
 cudaError_t launch_dw_reduce(const DwParams& p, const float* dy_scale, const float* x_scale, uint16_t* dW,
                              cudaStream_t s) {
-  dw_reduce_kernel<<<dim3(p.m_tiles * p.n_tiles, p.bn / 32), 256, 0, s>>>(p, dy_scale, x_scale, dW);
+  if (p.splits > kMaxReduceSplits) return cudaErrorInvalidValue;
+  dw_reduce_kernel<<<dim3(p.m_tiles * p.n_tiles, p.bn / 4), 128, 0, s>>>(p, dy_scale, x_scale, dW);
   return cudaGetLastError();
 }
 

@@ -69,8 +69,20 @@ __global__ void __launch_bounds__(1024) bank_amax_kernel(const __grid_constant__
   const int row_chunks = a.D / 8;  // 16-byte chunks per row
   const int64_t total = static_cast<int64_t>(a.N) * row_chunks;
   float m = 0.f;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < total; i += 4 * stride) {  // four independent loads in flight
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t e = i + j * stride;
+      v[j] = __ldg(reinterpret_cast<const uint4*>(bank_row(a, l, static_cast<int>(e / row_chunks))) +
+                   static_cast<int>(e % row_chunks));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, absmax_bf16x8(v[j]));
+  }
+  for (; i < total; i += stride) {
     const int n = static_cast<int>(i / row_chunks), c = static_cast<int>(i % row_chunks);
     m = fmaxf(m, absmax_bf16x8(__ldg(reinterpret_cast<const uint4*>(bank_row(a, l, n)) + c)));
   }

@@ -170,8 +170,9 @@ def selftest_wait_timeout(ws: torch.Tensor, timeout_us: int):
 
 
 def build_rope_table(max_pos: int, d_qk: int, base: float = 10000.0, device="cuda") -> torch.Tensor:
-    """cos/sin table [d_qk/2, max_pos, 2] float32 for RoPE."""
-    t = torch.empty((d_qk // 2, max_pos, 2), dtype=torch.float32, device=device)
+    """RoPE table [d_qk/4, max_pos, 4] float32: entry (j, p) holds
+    cos(p w_2j), cos(p w_2j+1), sin(p w_2j), sin(p w_2j+1)."""
+    t = torch.empty((d_qk // 4, max_pos, 4), dtype=torch.float32, device=device)
     _check(lib().qkvp_build_rope_table(_ptr(t), max_pos, d_qk, base, _stream(t.device)), "qkvp_build_rope_table")
     return t
 
@@ -274,7 +275,7 @@ def forward(x, pos, W8, w_scale, H, rope_table, d_qk=96, d_v=128, eps=1e-6, ws=N
     _need_cuda(W8, "W8", torch.uint8, (shape.N, D))
     _need_cuda(w_scale, "w_scale", torch.float32, (1,))
     _need_cuda(rope_table, "rope_table", torch.float32)
-    if rope_table.dim() != 3 or rope_table.shape[0] != d_qk // 2 or rope_table.shape[2] != 2:
+    if rope_table.dim() != 3 or rope_table.shape[0] != d_qk // 4 or rope_table.shape[2] != 4:
         raise ValueError("rope_table must be build_rope_table(max_pos, d_qk)")
     dev = x.device
     if ws is None:
@@ -320,6 +321,8 @@ def backward(dq, dk, dv, saved: Saved, W8T, w_scale, rope_table, ws=None, out=No
     _need_cuda(W8T, "W8T", torch.uint8, (D, shape.N))
     _need_cuda(w_scale, "w_scale", torch.float32, (1,))
     _need_cuda(rope_table, "rope_table", torch.float32)
+    if rope_table.dim() != 3 or rope_table.shape[0] != d_qk // 4 or rope_table.shape[2] != 4:
+        raise ValueError("rope_table must be build_rope_table(max_pos, d_qk)")
     dev = dq.device
     if ws is None:
         ws = new_workspace(shape, dev)

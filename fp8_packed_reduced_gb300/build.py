@@ -45,7 +45,8 @@ def _headers_mtime():
 def _compile(src: str, extra, verbose: bool) -> str:
     obj = os.path.join(BUILD, src[:-3] + ".o")
     srcp = os.path.join(CSRC, src)
-    if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(srcp), _headers_mtime()):
+    fresh = os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(srcp), _headers_mtime())
+    if fresh and not extra:
         return obj
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", srcp, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -13,16 +13,16 @@
 // inverse rotation of (g_out - mu * o) suffices).  dY_v = dv.
 //
 // Work unit: 128 tokens x one head x one part (q, k or v).  Persistent CTA
-// per SM, warp-specialised:
-//   warp 0       TMA producer: the unit's input boxes ([128 tokens x 32 cols],
-//                64-byte swizzle) into a ring of kBwdStages stages
-//   warps 1-16   two consumer groups of eight warps; group g takes every
-//                other unit of the CTA.  Two threads per token row: thread
-//                half h owns the 8-column blocks (c / 8) % 2 == h of the row,
-//                which keeps each rotation pair (i, i + d/2) in one thread;
-//                the row's mean(g_out * o) is one shuffle between the two.
-//                Pass 2 stages the codes of its unit (32-byte swizzle) and
-//                stores them by TMA while the other group computes.
+// per SM of two groups of eight warps; group g takes every other unit of the
+// CTA and owns its own ring of input stages, which one of its threads refills
+// by TMA (the unit's [128 tokens x 32 cols] boxes, 64-byte swizzle) as soon
+// as the group has read a stage.  Two threads per token row: thread half h
+// owns the 8-column blocks (c / 8) % 2 == h of the row, which keeps each
+// rotation pair (i, i + d/2) in one thread; the row's mean(g_out * o) is one
+// shuffle between the two.  A thread's RoPE factors for a unit are loaded
+// before its stage is awaited, and the saved rstd and position one unit
+// ahead.  Pass 2 stages the codes of its unit (32-byte swizzle) and stores
+// them by TMA while the other group computes.
 // Within a warp, lanes map to rows so that the 16-byte reads of a quarter
 // warp hit eight distinct 16-byte bank groups of the swizzled boxes.
 #include "kernels.cuh"
@@ -32,15 +32,17 @@ namespace qkvp {
 constexpr int kInBox = 8192;        // 128 rows x 32 bf16
 constexpr int kOutBox = 4096;       // 128 rows x 32 codes
 constexpr int kGroupThreads = 256;
-constexpr int kBwdThreads = 32 + 2 * kGroupThreads;
+constexpr int kBwdThreads = 2 * kGroupThreads;
+constexpr int kMaxStagesPerGroup = 3;
 
 __host__ __device__ constexpr int bwd_stage_bytes(int d_qk) {
   return (2 * d_qk > 128 ? 2 * d_qk : 128) / 32 * kInBox;   // max(dq+q, dv) boxes
 }
-// As many stages as fit beside the code staging: 4 at d_qk <= 96, 3 at 128.
-__host__ __device__ constexpr int bwd_stages(int d_qk) { return d_qk <= 96 ? 4 : 3; }
+// Input stages owned by each consumer group, as many as fit beside the code
+// staging: 3 at d_qk = 64 (32 KB stages), 2 at 96 (48 KB), 1 at 128 (64 KB).
+__host__ __device__ constexpr int bwd_stages_per_group(int d_qk) { return d_qk <= 64 ? 3 : d_qk <= 96 ? 2 : 1; }
 __host__ __device__ constexpr int bwd_smem_bytes(int d_qk, bool quant) {
-  return 1024 + bwd_stages(d_qk) * bwd_stage_bytes(d_qk) + (quant ? 2 * 4 * kOutBox : 0);
+  return 1024 + 2 * bwd_stages_per_group(d_qk) * bwd_stage_bytes(d_qk) + (quant ? 2 * 4 * kOutBox : 0);
 }
 
 struct BwdUnit {
@@ -73,50 +75,48 @@ __device__ __forceinline__ uint4 load8(const uint8_t* boxes, int r, int c) {
   return *reinterpret_cast<const uint4*>(boxes + (c >> 5) * kInBox + r * 64 + ((cc ^ ((r >> 1) & 3)) << 4));
 }
 
-__device__ __forceinline__ void unpack8(uint4 x, float (&v)[8]) {
-  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = bf16_lo(w[i]);
-    v[2 * i + 1] = bf16_hi(w[i]);
-  }
+
+// acc + the products of the eight bf16 of a with those of b, on two lanes
+__device__ __forceinline__ f2 dot8(uint4 a, uint4 b, f2 acc) {
+  acc = f2_fma(f2_from_bf16x2(a.x), f2_from_bf16x2(b.x), acc);
+  acc = f2_fma(f2_from_bf16x2(a.y), f2_from_bf16x2(b.y), acc);
+  acc = f2_fma(f2_from_bf16x2(a.z), f2_from_bf16x2(b.z), acc);
+  return f2_fma(f2_from_bf16x2(a.w), f2_from_bf16x2(b.w), acc);
 }
 
-__device__ __forceinline__ float dot8(uint4 a, uint4 b) {
-  float x[8], y[8];
-  unpack8(a, x);
-  unpack8(b, y);
-  float d = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) d = fmaf(x[i], y[i], d);
-  return d;
+// per-half unsigned 16-bit max
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // Eight codes of columns [c, c + 8) (c % 8 == 0) of row r into the
 // token-major staging boxes [128 rows][32 codes] with 32-byte swizzling
 // (the 16-byte half of a row is XORed with bit 2 of the row).
-__device__ __forceinline__ void emit8(const float (&v)[8], const Bracket& k, int r, int c, uint8_t* out8) {
-  const uint2 w = make_uint2(quant4_fast(v[0], v[1], v[2], v[3], k), quant4_fast(v[4], v[5], v[6], v[7], k));
+__device__ __forceinline__ void emit8(const f2 (&v)[4], const Bracket2& k, int r, int c, uint8_t* out8) {
+  const uint2 w = quant8(v, k);
   const int cl = c & 31;
   *reinterpret_cast<uint2*>(out8 + (c >> 5) * kOutBox + r * 32 + (((cl >> 4) ^ ((r >> 2) & 1)) << 4) + (cl & 15)) = w;
 }
 
-// Per-row saved state of a q/k unit: rstd and position (checked).
-__device__ __forceinline__ void row_state(const BwdParams& p, const BwdUnit& b, int t, float& rstd, int& pos,
-                                          const DevStatus& st, int kid) {
+// Issue the loads of a q/k unit's per-row saved state: rstd and position
+// (0 for rows past T; the position is range-checked where it is used).
+__device__ __forceinline__ void row_state(const BwdParams& p, const BwdUnit& b, int t, float& rstd, int& pos) {
   rstd = 0.f;
   pos = 0;
   if (t >= p.T) return;
   rstd = __ldg(p.rstd + (static_cast<int64_t>(b.part) * p.H + b.h) * p.T + t);
   pos = __ldg(p.pos + t);
-  if (pos < 0 || pos >= p.max_pos) {
-    record_error(st, QKVP_ERR_DEVICE_INPUT, kid);
-    pos = 0;
-  }
 }
 
 __device__ __forceinline__ void group_sync(int g) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(kGroupThreads) : "memory");
+}
+// The same barrier, placed after `dep` is computed: a value derived from
+// shared-memory reads pins those reads before the barrier in issue order.
+__device__ __forceinline__ void group_sync_after(int g, float dep) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(kGroupThreads), "f"(dep) : "memory");
 }
 
 // AND of `v` over the threads of consumer group g (all of them call it), so
@@ -134,160 +134,203 @@ __device__ __forceinline__ bool group_all(int g, bool v) {
   return out != 0;
 }
 
+// Pass 2: the group's previous TMA store has finished reading its code
+// staging, which the group is about to overwrite.
+__device__ __forceinline__ void staging_free(int g, int gt) {
+  if (gt == 0) bulk_wait_read<0>();
+  group_sync(g);
+}
+
 // One kernel body for both passes.  QUANT = false: amax partials; true: codes.
 template <int DQK, bool QUANT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_epi_kernel(const __grid_constant__ BwdMaps m, const __grid_constant__ BwdParams p, DevStatus st) {
   constexpr int kid = QUANT ? KID_BWD_QUANT : KID_BWD_AMAX;
   constexpr int kStage = bwd_stage_bytes(DQK);
-  constexpr int kBwdStages = bwd_stages(DQK);
+  constexpr int SPG = bwd_stages_per_group(DQK);
   constexpr int HALF = DQK / 2;      // rotation pairs per row
   constexpr int NG = HALF / 16;      // 16-pair groups; this thread owns 8 pairs of each
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[4], empty[4];
+  __shared__ __align__(8) uint64_t full[2 * kMaxStagesPerGroup];
   __shared__ float red[32];
   __shared__ int abort_flag;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = threadIdx.x / kGroupThreads;    // consumer group
+  const int gt = threadIdx.x % kGroupThreads;   // thread index inside the group
+  int r, hf;
+  row_and_half(gt, r, hf);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kBwdStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGroupThreads);
-    }
+    for (int s = 0; s < 2 * SPG; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
   }
   __syncthreads();
 
-  Bracket kq{1.f, 1.f, 1.f};
+  Bracket2 kq{1.f, 0, 0};
   if (QUANT) {
     const float s_dy = scale_from_amax(block_reduce_partials(p.partials, p.nparts, red));
-    kq = make_bracket(s_dy);
+    kq = make_bracket2(s_dy);
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.dy_scale = s_dy;
   }
 
-  float mx = 0.f;
-  if (warp == 0) {
-    if (lane == 0) {
-      int it = 0;
-      uint32_t used = 0, last_par = 0;  // stages filled; parity of their last fill
-      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
-        const int s = it % kBwdStages;
-        if (!mbar_wait(&empty[s], ((it / kBwdStages) & 1) ^ 1, &abort_flag, st, kid)) break;
-        used |= 1u << s;
-        last_par = (last_par & ~(1u << s)) | (static_cast<uint32_t>((it / kBwdStages) & 1) << s);
-        const BwdUnit b = bwd_decode(p, u);
-        uint8_t* in0 = smem + s * kStage;
-        const int d = b.part < 2 ? DQK : p.d_v;
-        const int nbox = d / 32;
-        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>((b.part < 2 ? 2 : 1) * nbox * kInBox));
-        const CUtensorMap* gm = b.part == 0 ? &m.dq : b.part == 1 ? &m.dk : &m.dv;
-        for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + j * kInBox, gm, &full[s], 32 * j, b.t0, b.h);
-        if (b.part < 2) {
-          const CUtensorMap* om = b.part == 0 ? &m.q : &m.k;
-          for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + (nbox + j) * kInBox, om, &full[s], 32 * j, b.t0, b.h);
-        }
-      }
-      // every copy issued has landed before the CTA may exit
-      for (int s = 0; s < kBwdStages; ++s)
-        if (used & (1u << s)) mbar_wait(&full[s], (last_par >> s) & 1, nullptr, st, kid);
+  uint8_t* stages = smem + g * SPG * kStage;                 // this group's input stages
+  uint8_t* out8 = smem + 2 * SPG * kStage + g * 4 * kOutBox;  // and its code staging
+  uint64_t* gfull = full + g * SPG;
+  const int ustep = 2 * gridDim.x;
+  // Input loads of unit u into stage s (thread gt == 0 only).  `inflight`
+  // and `inpar` record the stages whose loads have not been waited for.
+  uint32_t inflight = 0, inpar = 0;
+  auto load_unit = [&](int u, int s, uint32_t par) {
+    const BwdUnit b = bwd_decode(p, u);
+    uint8_t* in0 = stages + s * kStage;
+    const int nbox = (b.part < 2 ? DQK : p.d_v) / 32;
+    mbar_arrive_expect_tx(&gfull[s], static_cast<uint32_t>((b.part < 2 ? 2 : 1) * nbox * kInBox));
+    const CUtensorMap* gm = b.part == 0 ? &m.dq : b.part == 1 ? &m.dk : &m.dv;
+    for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + j * kInBox, gm, &gfull[s], 32 * j, b.t0, b.h);
+    if (b.part < 2) {
+      const CUtensorMap* om = b.part == 0 ? &m.q : &m.k;
+      for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + (nbox + j) * kInBox, om, &gfull[s], 32 * j, b.t0, b.h);
     }
-  } else {
-    const int g = (warp - 1) >> 3;                            // consumer group
-    const int gt = threadIdx.x - 32 - g * kGroupThreads;      // thread index inside the group
-    int r, hf;
-    row_and_half(gt, r, hf);
-    uint8_t* out8 = smem + kBwdStages * kStage + g * 4 * kOutBox;
-    const float2* rope = reinterpret_cast<const float2*>(p.rope);
-    int it = g;
-    for (int u = blockIdx.x + g * gridDim.x; u < p.num_units; u += 2 * gridDim.x, it += 2) {
-      const int s = it % kBwdStages;
-      const BwdUnit b = bwd_decode(p, u);
-      const int t = b.t0 + r;
-      const bool valid = t < p.T;
-      float rstd;
-      int pos;
-      if (b.part < 2) row_state(p, b, t, rstd, pos, st, kid);
-      if (QUANT) {
-        // the previous unit's stores have read this group's staging tiles
-        if (gt == 0) bulk_wait_read<0>();
-        group_sync(g);
+    inflight |= 1u << s;
+    inpar = (inpar & ~(1u << s)) | (par << s);
+  };
+  const int u0 = blockIdx.x + g * gridDim.x;
+  if (gt == 0)
+    for (int k = 0; k < SPG; ++k)
+      if (u0 + k * ustep < p.num_units) load_unit(u0 + k * ustep, k, 0);
+
+  float mx = 0.f;
+  const float4* rope = reinterpret_cast<const float4*>(p.rope);
+  // the saved state of the group's next q/k unit is loaded one unit ahead
+  float rstd_next = 0.f;
+  int pos_next = 0;
+  if (u0 < p.num_units) {
+    const BwdUnit b0 = bwd_decode(p, u0);
+    if (b0.part < 2) row_state(p, b0, b0.t0 + r, rstd_next, pos_next);
+  }
+  int k = 0;
+  for (int u = u0; u < p.num_units; u += ustep, ++k) {
+    const int s = k % SPG;
+    const uint32_t par = (k / SPG) & 1;
+    const BwdUnit b = bwd_decode(p, u);
+    const float rstd = rstd_next;
+    int pos = pos_next;
+    // this unit's RoPE factors, in flight while the stage arrives and the
+    // row's mean is formed
+    // entry w of group gg: cos, cos, sin, sin of pairs c + 2w, c + 2w + 1
+    float4 k4[NG][4];
+    if (b.part < 2) {
+      if (pos < 0 || pos >= p.max_pos) {
+        record_error(st, QKVP_ERR_DEVICE_INPUT, kid);
+        pos = 0;
       }
-      if (!group_all(g, mbar_wait(&full[s], (it / kBwdStages) & 1, &abort_flag, st, kid))) break;
-      const uint8_t* in0 = smem + s * kStage;
-      int nbox;
-      if (b.part < 2) {
-        const uint8_t* in1 = in0 + (DQK / 32) * kInBox;
-        const float2* rope_row = rope + pos;
-        float dot = 0.f;
+      const float4* rope_row = rope + pos;
 #pragma unroll
-        for (int gg = 0; gg < NG; ++gg) {
-          const int c = 16 * gg + 8 * hf;
-          dot += dot8(load8(in0, r, c), load8(in1, r, c)) + dot8(load8(in0, r, HALF + c), load8(in1, r, HALF + c));
+      for (int gg = 0; gg < NG; ++gg)
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          k4[gg][w] = __ldg(rope_row + static_cast<int64_t>(8 * gg + 4 * hf + w) * p.max_pos);
+    }
+    if (u + ustep < p.num_units) {
+      const BwdUnit bn = bwd_decode(p, u + ustep);
+      if (bn.part < 2) row_state(p, bn, bn.t0 + r, rstd_next, pos_next);
+    }
+    if (!group_all(g, mbar_wait(&gfull[s], par, &abort_flag, st, kid))) break;
+    if (gt == 0) inflight &= ~(1u << s);
+    const uint8_t* in0 = stages + s * kStage;
+    int nbox;
+    if (b.part < 2) {
+      const uint8_t* in1 = in0 + (DQK / 32) * kInBox;
+      f2 acc = 0;
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) {
+        const int c = 16 * gg + 8 * hf;
+        acc = dot8(load8(in0, r, c), load8(in1, r, c), acc);
+        acc = dot8(load8(in0, r, HALF + c), load8(in1, r, HALF + c), acc);
+        asm volatile("" ::: "memory");   // bounds the reads in flight (registers)
+      }
+      const float2 a2 = f2_split(acc);
+      float dot = a2.x + a2.y;
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);   // the row's other half
+      const float mu = __fdiv_rn(dot, static_cast<float>(DQK));
+      const f2 nmu = f2_make(-mu, -mu), rr = f2_make(rstd, rstd);
+      if (QUANT) staging_free(g, gt);
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) {
+        const int c = 16 * gg + 8 * hf;
+        const uint4 ga = load8(in0, r, c), gb = load8(in0, r, HALF + c);
+        const uint4 oa = load8(in1, r, c), ob = load8(in1, r, HALF + c);
+        const uint32_t gaw[4] = {ga.x, ga.y, ga.z, ga.w}, gbw[4] = {gb.x, gb.y, gb.z, gb.w};
+        const uint32_t oaw[4] = {oa.x, oa.y, oa.z, oa.w}, obw[4] = {ob.x, ob.y, ob.z, ob.w};
+        f2 ya[4], yb[4];   // dY of columns c + [0, 8) and HALF + c + [0, 8), two per word
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          // u = g_out - mu * o over the pair's two columns, then the inverse rotation
+          const f2 ua = f2_fma(f2_from_bf16x2(oaw[w]), nmu, f2_from_bf16x2(gaw[w]));
+          const f2 ub = f2_fma(f2_from_bf16x2(obw[w]), nmu, f2_from_bf16x2(gbw[w]));
+          const f2 cs = f2_make(k4[gg][w].x, k4[gg][w].y), sn = f2_make(k4[gg][w].z, k4[gg][w].w);
+          ya[w] = f2_mul(f2_fma(ub, sn, f2_mul(ua, cs)), rr);
+          yb[w] = f2_mul(f2_sub(f2_mul(ub, cs), f2_mul(ua, sn)), rr);
         }
-        dot += __shfl_xor_sync(0xffffffffu, dot, 1);   // the row's other half
-        const float mu = __fdiv_rn(dot, static_cast<float>(DQK));
+        if (QUANT) {
+          emit8(ya, kq, r, c, out8);
+          emit8(yb, kq, r, HALF + c, out8);
+        } else {
 #pragma unroll
-        for (int gg = 0; gg < NG; ++gg) {
-          const int c = 16 * gg + 8 * hf;
-          float2 k2[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) k2[j] = __ldg(rope_row + static_cast<int64_t>(c + j) * p.max_pos);
-          float ga[8], gb[8], oa[8], ob[8], a[8], c2[8];
-          unpack8(load8(in0, r, c), ga);
-          unpack8(load8(in0, r, HALF + c), gb);
-          unpack8(load8(in1, r, c), oa);
-          unpack8(load8(in1, r, HALF + c), ob);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float ua = ga[j] - mu * oa[j];
-            const float ub = gb[j] - mu * ob[j];
-            a[j] = valid ? rstd * (ua * k2[j].x + ub * k2[j].y) : 0.f;
-            c2[j] = valid ? rstd * (ub * k2[j].x - ua * k2[j].y) : 0.f;
-          }
-          if (QUANT) {
-            emit8(a, kq, r, c, out8);
-            emit8(c2, kq, r, HALF + c, out8);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fmaxf(fabsf(a[j]), fabsf(c2[j])));
-          }
+          for (int w = 0; w < 4; ++w) mx = f2_absmax(f2_absmax(mx, ya[w]), yb[w]);
+          // keep the next group's shared-memory reads from being hoisted
+          // above this one (their registers would spill)
+          asm volatile("" ::: "memory");
         }
-        mbar_arrive(&empty[s]);  // this thread is done with the stage
-        nbox = DQK / 32;
-      } else {
-        uint4 x[8];
+      }
+      nbox = DQK / 32;
+      if (QUANT) fence_async_smem();
+      // every value read from the stage has been used by now (see the v path)
+      group_sync_after(g, mx);   // the stage is read (and, in pass 2, the codes are staged)
+      if (gt == 0 && u + SPG * ustep < p.num_units) load_unit(u + SPG * ustep, s, par ^ 1u);
+    } else {
+      uint4 x[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = load8(in0, r, 16 * q + 8 * hf);
-        mbar_arrive(&empty[s]);  // inputs now in registers
+      for (int q = 0; q < 8; ++q) x[q] = load8(in0, r, 16 * q + 8 * hf);
+      // The values are used before the group barrier below: a barrier does
+      // not wait for shared-memory reads still in flight, and the TMA refill
+      // it releases would race with them.
+      if (QUANT) {
+        staging_free(g, gt);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          float v[8];
-          unpack8(x[q], v);
-          if (!valid) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0.f;
-          }
-          if (QUANT) {
-            emit8(v, kq, r, 16 * q + 8 * hf, out8);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(v[j]));
-          }
+          const f2 v[4] = {f2_from_bf16x2(x[q].x), f2_from_bf16x2(x[q].y), f2_from_bf16x2(x[q].z),
+                           f2_from_bf16x2(x[q].w)};
+          emit8(v, kq, r, 16 * q + 8 * hf, out8);
         }
-        nbox = 4;
-      }
-      if (QUANT) {
         fence_async_smem();
-        group_sync(g);
-        if (gt == 0) {
-          for (int j = 0; j < nbox; ++j) tma_store_2d(&m.dy8, out8 + j * kOutBox, b.col0 + 32 * j, b.t0);
-          bulk_commit();
+      } else {
+        // |bf16| orders as its 15 magnitude bits: max over packed halves
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          m2 = umax16x2(m2, x[q].x & 0x7FFF7FFFu);
+          m2 = umax16x2(m2, x[q].y & 0x7FFF7FFFu);
+          m2 = umax16x2(m2, x[q].z & 0x7FFF7FFFu);
+          m2 = umax16x2(m2, x[q].w & 0x7FFF7FFFu);
         }
+        mx = fmax3(mx, bf16_lo(m2), bf16_hi(m2));
       }
+      group_sync_after(g, mx);   // the stage is read (and, in pass 2, the codes are staged)
+      if (gt == 0 && u + SPG * ustep < p.num_units) load_unit(u + SPG * ustep, s, par ^ 1u);
+      nbox = 4;
     }
-    if (QUANT && gt == 0) bulk_wait_all<0>();
+    if (QUANT && gt == 0) {
+      for (int j = 0; j < nbox; ++j) tma_store_2d(&m.dy8, out8 + j * kOutBox, b.col0 + 32 * j, b.t0);
+      bulk_commit();
+    }
+  }
+  if (gt == 0) {
+    if (QUANT) bulk_wait_all<0>();
+    // loads still in flight after an early exit land before the CTA ends
+    for (int s = 0; s < SPG; ++s)
+      if (inflight & (1u << s)) mbar_wait(&gfull[s], (inpar >> s) & 1, nullptr, st, kid);
   }
   if (!QUANT) {
     mx = block_max(mx, red);

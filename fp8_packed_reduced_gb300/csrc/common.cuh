@@ -70,13 +70,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with parity `parity` of `bar` has completed.  Bounded:
-// gives up after st.timeout_ns, or as soon as another role of the CTA has set
-// *abort.  On expiry records QKVP_ERR_TIMEOUT and sets *abort.  Returns true
-// when the phase completed.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                       const DevStatus& st, int kid) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Polling part of mbar_wait (below), kept out of line.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                   const DevStatus& st, int kid) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
@@ -89,6 +85,15 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, vo
       return false;
     }
   }
+}
+// Wait until the phase with parity `parity` of `bar` has completed.  Bounded:
+// gives up after st.timeout_ns, or as soon as another role of the CTA has set
+// *abort.  On expiry records QKVP_ERR_TIMEOUT and sets *abort.  Returns true
+// when the phase completed.  A phase that has already completed costs one
+// inline test.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const DevStatus& st,
+                                          int kid) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort, st, kid);
 }
 
 // ---------------------------------------------------------------------------
@@ -289,6 +294,89 @@ __device__ __forceinline__ uint32_t quant2_fast(float a, float b, const Bracket&
 // Four codes packed little-endian (a in the lowest byte).
 __device__ __forceinline__ uint32_t quant4_fast(float a, float b, float c, float d, const Bracket& k) {
   return quant2_fast(a, b, k) | (quant2_fast(c, d, k) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// Packed float32 pairs: two lanes of one 64-bit register, for the f32x2
+// arithmetic of sm_100 and later (each lane rounds exactly as the scalar
+// instruction does).
+// ---------------------------------------------------------------------------
+using f2 = uint64_t;
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(f2 a) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(a));
+  return r;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// a * b + c, one rounding per lane
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// The two bf16 of a word (low half first) as a float pair, exactly.
+__device__ __forceinline__ f2 f2_from_bf16x2(uint32_t w) {
+  return f2_make(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// Both lanes rounded to bf16 and packed (lane 0 in the low half).
+__device__ __forceinline__ uint32_t f2_to_bf16x2(f2 a) {
+  const float2 v = f2_split(a);
+  __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// max(a, b, c) (three-operand form of sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// Running max of |lane| over a pair.
+__device__ __forceinline__ float f2_absmax(float m, f2 a) {
+  const float2 v = f2_split(a);
+  return fmax3(m, fabsf(v.x), fabsf(v.y));
+}
+
+// Eight codes (little-endian, lane 0 of v[0] lowest) with the bracket test
+// made once for all eight; the exact division is taken only when a bracket
+// straddles a rounding boundary.
+static __device__ __noinline__ uint2 quant8_exact(f2 v0, f2 v1, f2 v2, f2 v3, float s) {
+  const float2 a = f2_split(v0), b = f2_split(v1), c = f2_split(v2), d = f2_split(v3);
+  return make_uint2(quant1(a.x, s) | (quant1(a.y, s) << 8) | (quant1(b.x, s) << 16) | (quant1(b.y, s) << 24),
+                    quant1(c.x, s) | (quant1(c.y, s) << 8) | (quant1(d.x, s) << 16) | (quant1(d.y, s) << 24));
+}
+struct Bracket2 {
+  float s;
+  f2 lo, hi;   // both lanes rs(1 - 2^-20), rs(1 + 2^-20)
+};
+__device__ __forceinline__ Bracket2 make_bracket2(float s) {
+  const Bracket k = make_bracket(s);
+  return Bracket2{s, f2_make(k.lo, k.lo), f2_make(k.hi, k.hi)};
+}
+__device__ __forceinline__ uint32_t cvt_e4m3x2(f2 a) {
+  const float2 v = f2_split(a);
+  return __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);   // .x in the low byte
+}
+__device__ __forceinline__ uint2 quant8(const f2 (&v)[4], const Bracket2& k) {
+  const uint32_t l0 = cvt_e4m3x2(f2_mul(v[0], k.lo)) | (cvt_e4m3x2(f2_mul(v[1], k.lo)) << 16);
+  const uint32_t l1 = cvt_e4m3x2(f2_mul(v[2], k.lo)) | (cvt_e4m3x2(f2_mul(v[3], k.lo)) << 16);
+  const uint32_t h0 = cvt_e4m3x2(f2_mul(v[0], k.hi)) | (cvt_e4m3x2(f2_mul(v[1], k.hi)) << 16);
+  const uint32_t h1 = cvt_e4m3x2(f2_mul(v[2], k.hi)) | (cvt_e4m3x2(f2_mul(v[3], k.hi)) << 16);
+  if (__builtin_expect(((l0 ^ h0) | (l1 ^ h1)) == 0, 1)) return make_uint2(l0, l1);
+  return quant8_exact(v[0], v[1], v[2], v[3], k.s);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

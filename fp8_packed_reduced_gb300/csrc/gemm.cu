@@ -149,7 +149,7 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&g.tfull[b], 1);
-      mbar_init(&g.tempty[b], 32 * EW);
+      mbar_init(&g.tempty[b], EW);   // one arrival per epilogue warp
     }
     mbar_init(&g.mma_done, 1);
     fence_mbar_init();
@@ -181,7 +181,8 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
       tc_fence_after();
       epi.process(u, tmem_base + static_cast<uint32_t>(buf * 256) + (static_cast<uint32_t>(qw * 32) << 16));
       tc_fence_before();
-      mbar_arrive(&g.tempty[buf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&g.tempty[buf]);
     }
     epi.finish();
   }
@@ -290,7 +291,7 @@ struct FwdEpi {
   // this thread's token and its row of the RoPE table
   int kind, head0, nh, t;
   bool valid;
-  const float2* rope_row;
+  const float4* rope_row;   // entry j of this token: cos, cos, sin, sin of pairs 2j, 2j + 1
 
   __device__ void prepare(int u) {
     const int m = u / p.n_tiles;
@@ -305,7 +306,7 @@ struct FwdEpi {
         pos = 0;
       }
     }
-    rope_row = reinterpret_cast<const float2*>(p.rope) + pos;
+    rope_row = reinterpret_cast<const float4*>(p.rope) + pos;
   }
 
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t* stage_) {
@@ -335,7 +336,7 @@ struct FwdEpi {
       uint8_t* buf = acquire();
       if (kind < 2) {
         // pass 1: sum of squares of the raw accumulators (scaled once below)
-        float ss = 0.f;
+        f2 ss2 = 0;
 #pragma unroll
         for (int c = 0; c < DQK / 32; ++c) {
           uint32_t raw[32];
@@ -343,29 +344,34 @@ struct FwdEpi {
           tmem_ld16(tacc + hh * DQK + 32 * c + 16, raw + 16);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ss = fmaf(__uint_as_float(raw[i]), __uint_as_float(raw[i]), ss);
+          for (int i = 0; i < 16; ++i) {
+            const f2 v = f2_make(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+            ss2 = f2_fma(v, v, ss2);
+          }
         }
-        ss *= sxw * sxw;
+        const float2 ssp = f2_split(ss2);
+        const float ss = (ssp.x + ssp.y) * (sxw * sxw);
         const float r = 1.0f / sqrtf(__fdiv_rn(ss, static_cast<float>(DQK)) + p.eps);
         if (valid) p.rstd[(static_cast<int64_t>(kind) * p.H + h) * p.T + t] = r;
-        const float f = sxw * r;   // accumulator -> normalised value
+        const f2 f = f2_make(sxw * r, sxw * r);   // accumulator -> normalised value
         // pass 2: rotate 16 pairs at a time, columns [16g, 16g+16) and [HALF+16g, HALF+16g+16)
 #pragma unroll
         for (int g = 0; g < HALF / 16; ++g) {
-          float2 cs[16];
+          float4 cs[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) cs[i] = __ldg(rope_row + static_cast<int64_t>(g * 16 + i) * p.max_pos);
+          for (int w = 0; w < 8; ++w) cs[w] = __ldg(rope_row + static_cast<int64_t>(g * 8 + w) * p.max_pos);
           uint32_t ra[16], rb[16];
           tmem_ld16(tacc + hh * DQK + g * 16, ra);
           tmem_ld16(tacc + hh * DQK + HALF + g * 16, rb);
           tmem_ld_wait();
           uint32_t lo[8], hi[8];
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const float a0 = __uint_as_float(ra[i]) * f, a1 = __uint_as_float(ra[i + 1]) * f;
-            const float b0 = __uint_as_float(rb[i]) * f, b1 = __uint_as_float(rb[i + 1]) * f;
-            lo[i / 2] = pack_bf16x2(a0 * cs[i].x - b0 * cs[i].y, a1 * cs[i + 1].x - b1 * cs[i + 1].y);
-            hi[i / 2] = pack_bf16x2(b0 * cs[i].x + a0 * cs[i].y, b1 * cs[i + 1].x + a1 * cs[i + 1].y);
+          for (int w = 0; w < 8; ++w) {
+            const f2 a = f2_mul(f2_make(__uint_as_float(ra[2 * w]), __uint_as_float(ra[2 * w + 1])), f);
+            const f2 b = f2_mul(f2_make(__uint_as_float(rb[2 * w]), __uint_as_float(rb[2 * w + 1])), f);
+            const f2 c = f2_make(cs[w].x, cs[w].y), sn = f2_make(cs[w].z, cs[w].w);
+            lo[w] = f2_to_bf16x2(f2_sub(f2_mul(a, c), f2_mul(b, sn)));   // a cos - b sin
+            hi[w] = f2_to_bf16x2(f2_fma(a, sn, f2_mul(b, c)));           // b cos + a sin
           }
           stage16(buf, lane, g * 16, lo);
           stage16(buf, lane, HALF + g * 16, hi);
@@ -385,13 +391,14 @@ struct FwdEpi {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld16(tacc + hh * 128 + hf * 64 + 16 * c, raw + 16 * c);
           tmem_ld_wait();
+          const f2 sc = f2_make(sxw, sxw);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint32_t w[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              w[i] = pack_bf16x2(__uint_as_float(raw[g * 16 + 2 * i]) * sxw,
-                                 __uint_as_float(raw[g * 16 + 2 * i + 1]) * sxw);
+              w[i] = f2_to_bf16x2(
+                  f2_mul(f2_make(__uint_as_float(raw[g * 16 + 2 * i]), __uint_as_float(raw[g * 16 + 2 * i + 1])), sc));
             stage16(buf, lane, hf * 64 + g * 16, w);
           }
         }

@@ -51,7 +51,7 @@ struct FwdParams {
   float eps;
   const float* x_scale;
   const float* w_scale;
-  const float* rope;  // [d_qk/2][max_pos] (cos, sin)
+  const float* rope;  // [d_qk/4][max_pos] (cos, cos, sin, sin) of two rotation pairs
   int max_pos;
   const int32_t* pos;
   float* rstd;        // [2, H, T]

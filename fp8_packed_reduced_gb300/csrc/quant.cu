@@ -199,25 +199,32 @@ cudaError_t launch_x_quant(const uint16_t* x, int64_t n, uint8_t* x8, const floa
 }
 
 // ---------------------------------------------------------------------------
-// RoPE table: table[(i * max_pos + p) * 2 + {0, 1}] = cos, sin of p * w_i.
+// RoPE table, two rotation pairs per entry:
+//   table[(j * max_pos + p) * 4 + {0, 1, 2, 3}]
+//     = cos(p w_2j), cos(p w_2j+1), sin(p w_2j), sin(p w_2j+1),
+// w_i = base^(-2 i / d_qk), j < d_qk / 4, computed in float64.
 // ---------------------------------------------------------------------------
-__global__ void rope_table_kernel(float* table, int max_pos, int half, int d_qk, double base) {
-  const int64_t n = static_cast<int64_t>(half) * max_pos;
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n;
-       j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(j / max_pos), p = static_cast<int>(j % max_pos);
-    const double w = pow(base, -2.0 * i / d_qk);
+__global__ void rope_table_kernel(float* table, int max_pos, int quarter, int d_qk, double base) {
+  const int64_t n = static_cast<int64_t>(quarter) * max_pos;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(e / max_pos), p = static_cast<int>(e % max_pos);
+    float4 out;
     double sn, cs;
-    sincos(static_cast<double>(p) * w, &sn, &cs);
-    table[2 * j] = static_cast<float>(cs);
-    table[2 * j + 1] = static_cast<float>(sn);
+    sincos(static_cast<double>(p) * pow(base, -2.0 * (2 * j) / d_qk), &sn, &cs);
+    out.x = static_cast<float>(cs);
+    out.z = static_cast<float>(sn);
+    sincos(static_cast<double>(p) * pow(base, -2.0 * (2 * j + 1) / d_qk), &sn, &cs);
+    out.y = static_cast<float>(cs);
+    out.w = static_cast<float>(sn);
+    reinterpret_cast<float4*>(table)[e] = out;
   }
 }
 
 cudaError_t launch_rope_table(float* table, int max_pos, int d_qk, double base, cudaStream_t s) {
-  const int64_t n = static_cast<int64_t>(d_qk / 2) * max_pos;
+  const int64_t n = static_cast<int64_t>(d_qk / 4) * max_pos;
   const int blocks = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  rope_table_kernel<<<blocks, 256, 0, s>>>(table, max_pos, d_qk / 2, d_qk, base);
+  rope_table_kernel<<<blocks, 256, 0, s>>>(table, max_pos, d_qk / 4, d_qk, base);
   return cudaGetLastError();
 }
 

@@ -89,11 +89,13 @@ int qkvp_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * recorded the error (0 when none). */
 int qkvp_poll_device_status(void* ws, int* where, void* stream);
 
-/* RoPE table: table[(i * max_pos + p) * 2 + {0, 1}] = cos, sin of p * w_i,
- * w_i = base^(-2 i / d_qk), i < d_qk/2, 0 <= p < max_pos, computed in float64
+/* RoPE table, two rotation pairs per 16-byte entry:
+ *   table[(j * max_pos + p) * 4 + {0, 1, 2, 3}]
+ *     = cos(p w_2j), cos(p w_2j+1), sin(p w_2j), sin(p w_2j+1),
+ * w_i = base^(-2 i / d_qk), j < d_qk/4, 0 <= p < max_pos, computed in float64
  * on the device and stored as float32 ("96 is enough", section "The change":
  * q, k = rope(q), rope(k); rotate-half form).
- *   table: device, d_qk/2 * max_pos * 2 floats. */
+ *   table: device, 16-byte aligned, d_qk/4 * max_pos * 4 floats. */
 int qkvp_build_rope_table(float* table, int max_pos, int d_qk, double base, void* stream);
 
 /* Bank refresh, once per optimizer update ("Track 1 ... packed FP8 attention",

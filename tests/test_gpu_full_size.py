@@ -85,3 +85,25 @@ def test_backward_full_codes_and_sampled_gradients(run):
     assert_close(f32(r["dx"][ROWS]), dYh @ oracle.dequantize(oW8, os_w), "dx")
     _, dW = oracle.grad_gemms(dY8, np.float32(r["dy_scale"]), oW8, os_w, x8, np.float32(r["x_scale"]))
     assert_close(f32(r["dW"]), dW, "dW")
+
+
+def test_backward_repeatable(run):
+    """Three more backward passes on the same inputs give bit-identical codes
+    and gradients: the stage ring, the code staging and the split-K reduction
+    leave no room for ordering races at this size."""
+    import fp8_packed_reduced_gb300 as qk
+    s, inp, g, r = run
+    dev_in = [g[n].to(DEV) for n in ("dq", "dk", "dv")]
+    saved = qk.Saved(q=r["q"].to(DEV), k=r["k"].to(DEV), rstd=r["rstd"].to(DEV), x8=r["x8"].to(DEV),
+                     x_scale=torch.tensor([r["x_scale"]], dtype=torch.float32, device=DEV),
+                     pos=inp["pos"].to(DEV))
+    W8T = torch.from_numpy(r["W8T"]).to(DEV)
+    w_scale = torch.tensor([r["w_scale"]], dtype=torch.float32, device=DEV)
+    table = qk.build_rope_table(s.seq_len, s.d_qk, 10000.0, DEV)
+    for _ in range(3):
+        out = qk.backward(*dev_in, saved, W8T, w_scale, table)
+        torch.cuda.synchronize()
+        assert out["dy_scale"].item() == r["dy_scale"]
+        assert torch.equal(out["dY8"].cpu(), r["dY8"])
+        assert torch.equal(out["dx"].cpu(), r["dx"])
+        assert torch.equal(out["dW"].cpu(), r["dW"])

@@ -168,6 +168,10 @@ def run_ours(args, rank, world):
     from fp8_packed_reduced_gb300 import build as b
     b.build()
     import fp8_packed_reduced_gb300 as qk
+    if args.cta_pairs is not None:
+        qk.set_cta_pairs(args.cta_pairs)
+    pairs = qk.set_cta_pairs(0)          # read the mask back
+    qk.set_cta_pairs(pairs)
     s = synth.Shape(T=args.T, D=args.D, H=args.H, d_qk=args.dqk, d_v=128, seq_len=args.seq_len)
     st = Step(s, dev)
     stream = torch.cuda.current_stream(dev)
@@ -268,7 +272,8 @@ def run_ours(args, rank, world):
         "config": {"workload": f"packed QKV fwd+bwd, T={s.T} ({s.T // s.seq_len}x{s.seq_len}), D={s.D}, "
                                f"H={s.H}, d_qk={s.d_qk}, d_v={s.d_v}, bank refresh per step",
                    "T": s.T, "D": s.D, "H": s.H, "d_qk": s.d_qk, "d_v": s.d_v, "parallelism": f"replicas{world}",
-                   "l2": "no flush; one step touches ~1.3 GB, 10x the 129 MB L2"},
+                   "l2": "no flush; one step touches ~1.3 GB, 10x the 129 MB L2",
+                   "gemm_cta_pairs": pairs},
         "roofline": roofline, "kernels": kern,
         "gpu_launches": len(KERNELS) * args.steps,
         "launch": "the K timed steps replayed as one captured CUDA graph",
@@ -387,6 +392,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=8192, help="tokens the oracle times for cpu_baseline")
     ap.add_argument("--ref-sample", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cta-pairs", type=int, default=None,
+                    help="GEMMs on 2-CTA clusters: bit 0 forward, bit 1 dX, bit 2 dW (default: the library's)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

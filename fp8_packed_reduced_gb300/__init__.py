@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "qkvp_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
             "qkvp_set_timing_events": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int]),
             "qkvp_timing_events_recorded": (ctypes.c_int, []),
+            "qkvp_set_cta_pairs": (ctypes.c_int, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -158,6 +159,15 @@ def set_timing_events(events):
 
 def timing_events_recorded() -> int:
     return int(lib().qkvp_timing_events_recorded())
+
+
+def set_cta_pairs(mask: int) -> int:
+    """Choose which GEMMs run on 2-CTA clusters (bit 0 forward, bit 1 dX,
+    bit 2 dW); returns the previous mask."""
+    prev = int(lib().qkvp_set_cta_pairs(mask))
+    if prev < 0:
+        raise ValueError(f"cta pair mask {mask} outside 0..7")
+    return prev
 
 
 def set_wait_timeout_ns(ns: int):

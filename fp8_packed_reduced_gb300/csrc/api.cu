@@ -13,6 +13,11 @@ using namespace qkvp;
 namespace {
 
 uint64_t g_timeout_ns = 2000000000ull;
+// GEMMs run on CTA pairs (bit 0 forward, bit 1 dX, bit 2 dW).  The dX and
+// dW GEMMs gain from pairs (their main loops are bound by shared-memory
+// bandwidth, which pairs relieve); the forward GEMM, bound by its epilogue,
+// does not.
+int g_pair_mask = 6;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -108,8 +113,9 @@ size_t ws_bytes_for(const qkvp_dims* d) {
   return kStatusBytes + 2 * kPartsBytes + dw_partial_bytes(dw_shape(d), kMaxSplits);
 }
 
-// Split count for the dW GEMM: the fewest splits whose units fill the SMs in
-// whole waves to >= 90%, with at least 4 k-blocks per split.
+// Split count for the dW GEMM: the fewest splits whose units fill the
+// workers (SMs, or SM pairs) in whole waves to >= 90%, with at least 4
+// k-blocks per split.
 int choose_splits(int tiles, int kblocks, int sms) {
   int best = 1;
   double best_eff = 0.0;
@@ -209,6 +215,13 @@ int qkvp_set_timing_events(void* const* events, int n) {
 
 int qkvp_timing_events_recorded(void) { return g_timing.next; }
 
+int qkvp_set_cta_pairs(int mask) {
+  if (mask < 0 || mask > 7) return -1;
+  const int prev = g_pair_mask;
+  g_pair_mask = mask;
+  return prev;
+}
+
 int qkvp_set_wait_timeout_ns(uint64_t ns) {
   if (ns < 1000000ull || ns > 60000000000ull) return QKVP_ERR_INVALID_ARGUMENT;
   g_timeout_ns = ns;
@@ -293,12 +306,15 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
 
   // Tiles of the packed GEMM cover whole heads: q/k tiles of hq heads (the
   // last one may hold fewer), v tiles of 2 heads.  Each stage loads B as one
-  // box of the full tile height: hq*d_qk rows (q/k) or 2*d_v rows (v).
+  // box of the full tile height, hq*d_qk rows (q/k) or 2*d_v rows (v), or
+  // on CTA pairs each CTA half of it.
   const int hq = dqk == 64 ? 4 : 2;
+  const int pair = (g_pair_mask & 1) ? 2 : 1;
   CUtensorMap tm_x8, tm_w, tm_wv, tm_q, tm_k, tm_v;
   bool ok = map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, hq * dqk, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, 2 * dv, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, hq * dqk / pair,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, 2 * dv / pair, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map3d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -321,7 +337,8 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.nq = (H + p.hq - 1) / p.hq;
   p.nv = (H + 1) / 2;
   p.n_tiles = 2 * p.nq + p.nv;
-  p.num_units = tiles * p.n_tiles;
+  p.pair = pair;
+  p.num_units = (tiles + pair - 1) / pair * p.n_tiles;
   p.kblocks = D / 128;
   p.eps = eps;
   p.x_scale = x_scale;
@@ -330,8 +347,7 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.max_pos = max_pos;
   p.pos = pos;
   p.rstd = rstd;
-  const int grid = std::min(p.num_units, sms);
-  QKVP_TRY_CUDA(launch_fwd_gemm(tm_x8, tm_w, tm_wv, tm_q, tm_k, tm_v, p, grid, st, s));
+  QKVP_TRY_CUDA(launch_fwd_gemm(tm_x8, tm_w, tm_wv, tm_q, tm_k, tm_v, p, sms, st, s));
   mark(s);
   return QKVP_OK;
 }
@@ -374,8 +390,10 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   // dY8 [T, N] read as 128 x 128 tiles: K-major A of the dX GEMM, MN-major A of the dW GEMM
   CUtensorMap tm_dy, tm_w8t, tm_dx, tm_x8;
   ok = ok && map2d(&tm_dy, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  const int dx_bn = D % 256 == 0 ? 256 : 128;   // one box per stage: the whole B tile
-  ok = ok && map2d(&tm_w8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8T, N, D, N, 128, dx_bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  const int dx_bn = D % 256 == 0 ? 256 : 128;   // one box per stage: the whole B tile (this CTA's half on pairs)
+  const int dx_pair = (g_pair_mask & 2) ? 2 : 1;
+  ok = ok && map2d(&tm_w8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8T, N, D, N, 128, dx_bn / dx_pair,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dx, D, T, D * 2ull, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return QKVP_ERR_CUDA;
@@ -406,11 +424,12 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   xp.D = D;
   xp.bn = dx_bn;
   xp.n_tiles = D / xp.bn;
-  xp.num_units = tiles * xp.n_tiles;
+  xp.pair = dx_pair;
+  xp.num_units = (tiles + dx_pair - 1) / dx_pair * xp.n_tiles;
   xp.kblocks = (N + 127) / 128;
   xp.dy_scale = dy_scale;
   xp.w_scale = w_scale;
-  QKVP_TRY_CUDA(launch_dx_gemm(tm_dy, tm_w8t, tm_dx, xp, std::min(xp.num_units, sms), st, s));
+  QKVP_TRY_CUDA(launch_dx_gemm(tm_dy, tm_w8t, tm_dx, xp, sms, st, s));
   mark(s);
 
   const DwShape ds = dw_shape(dims);
@@ -421,10 +440,13 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   wp.m_tiles = ds.m_tiles;
   wp.n_tiles = ds.n_tiles;
   wp.kblocks_total = ds.kblocks_total;
-  wp.splits = choose_splits(ds.m_tiles * ds.n_tiles, ds.kblocks_total, sms);
-  wp.num_units = wp.splits * ds.m_tiles * ds.n_tiles;
+  // pairs split the 256 columns of a tile: one 128-column box of x8 each
+  wp.pair = ((g_pair_mask & 4) && ds.bn == 256) ? 2 : 1;
+  const int pair_tiles = (ds.m_tiles + wp.pair - 1) / wp.pair * ds.n_tiles;
+  wp.splits = choose_splits(pair_tiles, ds.kblocks_total, sms / wp.pair);
+  wp.num_units = wp.splits * pair_tiles;
   wp.partials = dwparts;
-  QKVP_TRY_CUDA(launch_dw_gemm(tm_dy, tm_x8, wp, std::min(wp.num_units, sms), st, s));
+  QKVP_TRY_CUDA(launch_dw_gemm(tm_dy, tm_x8, wp, sms, st, s));
   mark(s);
   QKVP_TRY_CUDA(launch_dw_reduce(wp, dy_scale, x_scale, dW, s));
   mark(s);

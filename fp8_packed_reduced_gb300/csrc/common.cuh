@@ -70,14 +70,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test with acquire semantics at cluster scope (for phases completed
+// by arrivals from the other CTA of a pair).
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+template <bool CL>
+__device__ __forceinline__ bool mbar_try_wait_t(uint64_t* bar, uint32_t parity) {
+  return CL ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 // Polling part of mbar_wait (below), kept out of line.
+template <bool CL = false>
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                    const DevStatus& st, int kid) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_t<CL>(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
     if (globaltimer_ns() - t0 > st.timeout_ns) {
       record_error(st, QKVP_ERR_TIMEOUT, kid);
@@ -93,7 +112,12 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 // inline test.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const DevStatus& st,
                                           int kid) {
-  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort, st, kid);
+  return mbar_try_wait(bar, parity) || mbar_wait_slow<false>(bar, parity, abort, st, kid);
+}
+// mbar_wait with acquire semantics at cluster scope.
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort, const DevStatus& st,
+                                             int kid) {
+  return mbar_try_wait_cl(bar, parity) || mbar_wait_slow<true>(bar, parity, abort, st, kid);
 }
 
 // ---------------------------------------------------------------------------
@@ -105,6 +129,24 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "[%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+// The same load with the completion signalled on the mbarrier at
+// shared::cluster address `bar`; with CG2 (cta_group::2) that barrier may sit
+// in either CTA of a 2-CTA pair (the destination is this CTA's own memory).
+template <bool CG2>
+__device__ __forceinline__ void tma_load_2d_at(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  if (CG2)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                             int z) {
@@ -179,6 +221,87 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// The same operations for a pair of CTAs (a 2-CTA cluster) sharing one MMA
+// (cta_group::2): allocation and release are collective (one warp in each
+// CTA), the even CTA issues the MMAs (M = 256: A rows 0-127 from its shared
+// memory, 128-255 from its peer's at the same offsets; B's N columns split
+// in halves the same way; D rows land in each CTA's own TMEM lanes), and
+// commits arrive on the barrier at the same offset in both CTAs.  Every
+// tcgen05 operation of a kernel uses one CTA-group size, hence the template.
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc_t(uint32_t* dst_smem, uint32_t ncols) {
+  if (PAIR)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+  else
+    tmem_alloc(dst_smem, ncols);
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_relinquish_t() {
+  if (PAIR)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    tmem_relinquish();
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc_t(uint32_t taddr, uint32_t ncols) {
+  if (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    tmem_dealloc(taddr, ncols);
+}
+template <bool PAIR>
+__device__ __forceinline__ void umma_e4m3_t(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  if (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    umma_e4m3(d_tmem, adesc, bdesc, idesc, accumulate);
+}
+// Arrive on `bar` (in both CTAs of the pair for PAIR) once every MMA issued
+// so far by this thread has completed.
+template <bool PAIR>
+__device__ __forceinline__ void umma_commit_t(uint64_t* bar) {
+  if (PAIR)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+  else
+    umma_commit(bar);
+}
+
+// ---------------------------------------------------------------------------
+// Clusters
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; release/acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address, in the cluster's shared window, of this CTA's shared variable `p`
+// as it sits in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_rank(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrive (release at cluster scope) on an mbarrier given by its cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Instruction descriptor for kind::f8f6f4: D = F32, A = B = E4M3, both

@@ -17,8 +17,16 @@
 //              the unit's heads or columns), one accumulator row (token) per
 //              thread; TMEM holds two 256-column accumulators so the
 //              epilogue of one unit overlaps the MMAs of the next
+// On CTA pairs (a 2-CTA cluster, cta_group::2) a unit is a 256-row tile:
+// each CTA loads its own 128 rows of A and half of B (both halves complete
+// on the even CTA's stage barrier), the even CTA's MMA thread issues M = 256
+// MMAs over both CTAs' shared memory, each CTA's epilogue reads its own TMEM
+// rows, and the MMA commits arrive on both CTAs' barriers.  Per SM this halves
+// the shared-memory traffic of B (written by TMA, read by the MMA).
 // Every wait is bounded (see mbar_wait); on expiry the kernel records
 // QKVP_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <utility>
+
 #include "kernels.cuh"
 
 namespace qkvp {
@@ -26,7 +34,9 @@ namespace qkvp {
 constexpr int kBM = 128;                   // accumulator rows (tokens, or bank rows for dW)
 constexpr int kBK = 128;                   // K bytes per stage (E4M3: 128 elements)
 constexpr int kAStage = kBM * kBK;         // 16 KB
-constexpr int kBStage = 256 * kBK;         // 32 KB (largest B tile)
+// Dynamic shared memory a GEMM CTA may use: the 227 KB opt-in limit less
+// 1 KB for the static barriers.
+constexpr int kSmemMax = 232448 - 1024;
 // Threads of a GEMM CTA with EW epilogue warps (4 or 8).
 __host__ __device__ constexpr int gemm_threads(int ew) { return 64 + 32 * ew; }
 constexpr int kTmemCols = 512;             // 2 accumulators x 256 fp32 columns
@@ -39,7 +49,7 @@ struct Unit {
 };
 
 struct GemmSmem {
-  uint64_t full[kMaxStages];
+  uint64_t full[kMaxStages];    // a stage landed (in a pair: both CTAs' halves, on the even CTA's barrier)
   uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
@@ -48,27 +58,64 @@ struct GemmSmem {
   int abort_flag;
 };
 
+// The stage ring: `stages` slots of one A tile and one B tile of up to
+// `bstage` bytes (a multiple of 1024, the 128-byte swizzle atom).
+struct Ring {
+  int stages, bstage;
+};
+
 // Dynamic shared memory: alignment slack, the stage ring, and `epb` bytes of
 // output staging per epilogue warp (boxes of 32 rows x 64 B).
-__host__ __device__ constexpr int gemm_smem_bytes(int stages, int ew, int epb) {
-  return 1024 + stages * (kAStage + kBStage) + ew * epb;
+__host__ __device__ constexpr int gemm_smem_bytes(Ring r, int ew, int epb) {
+  return 1024 + r.stages * (kAStage + r.bstage) + ew * epb;
+}
+// As many stages of (A, `bstage`-byte B) as fit beside the staging.
+__host__ __device__ constexpr Ring ring_for(int bstage, int ew, int epb) {
+  return Ring{(kSmemMax - 1024 - ew * epb) / (kAStage + bstage) < kMaxStages
+                  ? (kSmemMax - 1024 - ew * epb) / (kAStage + bstage)
+                  : kMaxStages,
+              bstage};
+}
+
+// Units are distributed over CTAs, or over CTA pairs (2-CTA clusters, ranks
+// 0 and 1 at consecutive block indices) that compute one 256-row tile.
+template <bool PAIR>
+__device__ __forceinline__ int unit_first() {
+  return PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+}
+template <bool PAIR>
+__device__ __forceinline__ int unit_stride() {
+  return PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 }
 
 // ---------------------------------------------------------------------------
 // Producer and MMA roles (one thread each)
 // ---------------------------------------------------------------------------
-template <class Sched>
+// Loads this CTA's operand tiles (its A rows and, in a pair, its half of B).
+// In a pair both CTAs' copies of a stage complete on the even CTA's `full`
+// barrier, which the even CTA arms with the bytes of both halves (a copy of
+// the odd CTA may land before that arming: the phase cannot complete while
+// the arrival is missing).
+template <bool PAIR, class Sched>
 __device__ void producer_role(const Sched& sc, const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* sA,
-                              uint8_t* sB, GemmSmem& g, int stages, const DevStatus& st, int kid) {
+                              uint8_t* sB, GemmSmem& g, Ring ring, const DevStatus& st, int kid) {
+  const int stages = ring.stages;
+  const bool leader = !PAIR || cluster_rank() == 0;
+  const uint32_t full0 = PAIR ? mapa_rank(&g.full[0], 0) : smem_u32(&g.full[0]);
   int stage = 0;
   uint32_t phase = 0;
   uint32_t used = 0, last_par = 0;  // stages filled at least once; parity of their last fill
-  for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x) {
+  bool aborted = false;
+  for (int u = unit_first<PAIR>(); u < sc.num_units(); u += unit_stride<PAIR>()) {
     const Unit ui = sc.unit(u);
     for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
-      if (!mbar_wait(&g.empty[stage], phase ^ 1, &g.abort_flag, st, kid)) goto drain;
-      mbar_arrive_expect_tx(&g.full[stage], static_cast<uint32_t>(kAStage + ui.b_bytes));
-      sc.load(ui, kb, tmA, tmB, sA + stage * kAStage, sB + stage * kBStage, &g.full[stage]);
+      if (!mbar_wait(&g.empty[stage], phase ^ 1, &g.abort_flag, st, kid)) {
+        aborted = true;
+        goto drain;
+      }
+      if (leader) mbar_arrive_expect_tx(&g.full[stage], static_cast<uint32_t>((PAIR ? 2 : 1) * (kAStage + ui.b_bytes)));
+      sc.template load<PAIR>(ui, kb, tmA, tmB, sA + stage * kAStage, sB + stage * ring.bstage,
+                             full0 + 8u * static_cast<uint32_t>(stage));
       used |= 1u << stage;
       last_par = (last_par & ~(1u << stage)) | (phase << stage);
       if (++stage == stages) {
@@ -78,25 +125,40 @@ __device__ void producer_role(const Sched& sc, const CUtensorMap* tmA, const CUt
     }
   }
 drain:
-  // every copy this thread issued has landed before the CTA may exit
-  for (int s = 0; s < stages; ++s)
-    if (used & (1u << s)) mbar_wait(&g.full[s], (last_par >> s) & 1, nullptr, st, kid);
+  // every copy issued here has landed before the CTA may exit
+  if (leader) {
+    for (int s = 0; s < stages; ++s)
+      if (used & (1u << s)) mbar_wait(&g.full[s], (last_par >> s) & 1, nullptr, st, kid);
+  } else if (aborted) {
+    // The odd CTA cannot observe the even CTA's barrier: after an abort it
+    // waits 100 us, far longer than any copy from device memory takes.  (On
+    // the normal path the even CTA's MMAs consume every copy before the
+    // pair's final cluster barrier.)
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 100000ull) {
+    }
+  }
 }
 
-template <class Sched>
-__device__ void mma_role(const Sched& sc, uint8_t* sA, uint8_t* sB, GemmSmem& g, uint32_t tmem_base, int stages,
+// Issues the MMAs (the even CTA of a pair issues them for both CTAs, M = 256).
+template <bool PAIR, class Sched>
+__device__ void mma_role(const Sched& sc, uint8_t* sA, uint8_t* sB, GemmSmem& g, uint32_t tmem_base, Ring ring,
                          const DevStatus& st, int kid) {
+  const int stages = ring.stages;
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
-  for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x, ++it) {
+  for (int u = unit_first<PAIR>(); u < sc.num_units(); u += unit_stride<PAIR>(), ++it) {
     const Unit ui = sc.unit(u);
     const int buf = it & 1;
     const uint32_t use = (it >> 1) & 1;
-    if (!mbar_wait(&g.tempty[buf], use ^ 1, &g.abort_flag, st, kid)) break;
+    // both CTAs' epilogues have read this accumulator buffer
+    if (!(PAIR ? mbar_wait_cl(&g.tempty[buf], use ^ 1, &g.abort_flag, st, kid)
+               : mbar_wait(&g.tempty[buf], use ^ 1, &g.abort_flag, st, kid)))
+      break;
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + buf * 256;
-    const uint32_t idesc = idesc_e4m3_f32_major(kBM, ui.ncols, Sched::kMN, Sched::kMN);
+    const uint32_t idesc = idesc_e4m3_f32_major(PAIR ? 2 * kBM : kBM, ui.ncols, Sched::kMN, Sched::kMN);
     bool ok = true;
     for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
       if (!mbar_wait(&g.full[stage], phase, &g.abort_flag, st, kid)) {
@@ -104,42 +166,45 @@ __device__ void mma_role(const Sched& sc, uint8_t* sA, uint8_t* sB, GemmSmem& g,
         break;
       }
       tc_fence_after();
-      const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBStage);
+      const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * ring.bstage);
 #pragma unroll
       for (int kk = 0; kk < kBK / 32; ++kk) {
         // K = 32 per instruction: 32 bytes along a K-major row, or 32 rows
         // (four 8-row atoms) of an MN-major tile
         const uint64_t ad = Sched::kMN ? sdesc_sw128(a0 + kk * 4096, 16384, 1024) : sdesc_k_sw128(a0 + kk * 32);
         const uint64_t bd = Sched::kMN ? sdesc_sw128(b0 + kk * 4096, 16384, 1024) : sdesc_k_sw128(b0 + kk * 32);
-        umma_e4m3(d_tmem, ad, bd, idesc, (kb > ui.kb0 || kk > 0) ? 1u : 0u);
+        umma_e4m3_t<PAIR>(d_tmem, ad, bd, idesc, (kb > ui.kb0 || kk > 0) ? 1u : 0u);
       }
-      umma_commit(&g.empty[stage]);
+      umma_commit_t<PAIR>(&g.empty[stage]);
       if (++stage == stages) {
         stage = 0;
         phase ^= 1;
       }
     }
     if (!ok) break;
-    umma_commit(&g.tfull[buf]);
+    umma_commit_t<PAIR>(&g.tfull[buf]);
   }
   // all MMAs issued by this thread have completed before TMEM is freed
-  umma_commit(&g.mma_done);
+  umma_commit_t<PAIR>(&g.mma_done);
   mbar_wait(&g.mma_done, 0, nullptr, st, kid);
 }
+
 
 // ---------------------------------------------------------------------------
 // Common body
 // ---------------------------------------------------------------------------
-template <int EW, int EPB, class Sched, class Epi>
+template <int EW, int EPB, bool PAIR, class Sched, class Epi>
 __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUtensorMap* tmA,
-                                          const CUtensorMap* tmB, int stages, const DevStatus& st, int kid) {
+                                          const CUtensorMap* tmB, Ring ring, const DevStatus& st, int kid) {
+  const int stages = ring.stages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ GemmSmem g;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + stages * kAStage;
-  uint8_t* sE = sB + stages * kBStage;
+  uint8_t* sE = sB + stages * ring.bstage;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool leader = !PAIR || cluster_rank() == 0;
 
   if (threadIdx.x == 0) {
     g.abort_flag = 0;
@@ -149,7 +214,7 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&g.tfull[b], 1);
-      mbar_init(&g.tempty[b], EW);   // one arrival per epilogue warp
+      mbar_init(&g.tempty[b], PAIR ? 2 * EW : EW);   // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(&g.mma_done, 1);
     fence_mbar_init();
@@ -157,24 +222,31 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
     prefetch_tmap(tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&g.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_t<PAIR>(&g.tmem_base, kTmemCols);
+    tmem_relinquish_t<PAIR>();
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();   // the peer's barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = g.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role(sc, tmA, tmB, sA, sB, g, stages, st, kid);
+    if (lane == 0) producer_role<PAIR>(sc, tmA, tmB, sA, sB, g, ring, st, kid);
   } else if (warp == 1) {
-    if (lane == 0) mma_role(sc, sA, sB, g, tmem_base, stages, st, kid);
+    if (lane == 0) {
+      if (leader)
+        mma_role<PAIR>(sc, sA, sB, g, tmem_base, ring, st, kid);
+      else   // the odd CTA's memory and TMEM stay in use until the pair's MMAs are done
+        mbar_wait(&g.mma_done, 0, nullptr, st, kid);
+    }
   } else {
     const int qw = warp & 3;          // TMEM lane quarter this warp may access
     const int sub = (warp - 2) >> 2;  // which share of the unit's heads / columns
     epi.begin(qw, sub, EW / 4, lane, sE + (warp - 2) * EPB);
+    const uint32_t tempty0 = PAIR ? mapa_rank(&g.tempty[0], 0) : 0;
     int it = 0;
-    for (int u = blockIdx.x; u < sc.num_units(); u += gridDim.x, ++it) {
+    for (int u = unit_first<PAIR>(); u < sc.num_units(); u += unit_stride<PAIR>(), ++it) {
       const int buf = it & 1;
       epi.prepare(u);  // loads that do not depend on the accumulator
       if (!mbar_wait(&g.tfull[buf], (it >> 1) & 1, &g.abort_flag, st, kid)) break;
@@ -182,14 +254,20 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
       epi.process(u, tmem_base + static_cast<uint32_t>(buf * 256) + (static_cast<uint32_t>(qw * 32) << 16));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&g.tempty[buf]);
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(tempty0 + 8u * static_cast<uint32_t>(buf));
+        else
+          mbar_arrive(&g.tempty[buf]);
+      }
     }
     epi.finish();
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();   // neither CTA leaves while the other may still address it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tmem_dealloc_t<PAIR>(tmem_base, kTmemCols);
 }
 
 // 16-byte chunk `col / 8` of row `row` in a staging box of 32 rows x 32
@@ -207,16 +285,6 @@ __device__ __forceinline__ void stage16(uint8_t* boxes, int row, int c0, const u
   stage_chunk_sw64(box, row, (c0 & 31) + 8, make_uint4(w[4], w[5], w[6], w[7]));
 }
 
-// K-major operands: A is one box of 128 rows x 128 bytes of K at (k, a_row);
-// B is ncols/R boxes of R rows x 128 bytes at (k, b_row + R j), R = b_rows
-// (the B tensor map's box height).
-__device__ __forceinline__ void load_k_major(const Unit& ui, int kb, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                             uint8_t* sA, uint8_t* sB, uint64_t* bar, int b_rows) {
-  tma_load_2d(sA, tmA, bar, kb * kBK, ui.a_row);
-  for (int j = 0; j < ui.ncols / b_rows; ++j)
-    tma_load_2d(sB + j * b_rows * kBK, tmB, bar, kb * kBK, ui.b_row + b_rows * j);
-}
-
 // ---------------------------------------------------------------------------
 // Forward: schedule and epilogue
 // ---------------------------------------------------------------------------
@@ -224,12 +292,18 @@ struct FwdSched {
   static constexpr bool kMN = false;
   const FwdParams& p;
   const CUtensorMap* tmBv;   // W8 with the v tiles' box height (the q/k one is the body's B map)
+  int rank, pair;            // CTA within its pair (0 when unpaired), CTAs per unit (1 or 2)
+  // 128-row block of tokens this CTA computes for unit u
+  __device__ int mtile(int u) const { return (u / p.n_tiles) * pair + rank; }
   // B: one box per stage, hq*d_qk rows for q/k tiles and 2*d_v rows for v
-  // tiles (a narrower last tile receives the whole box; the MMA uses ncols).
+  // tiles, or in a pair this CTA's half of them (starting ncols/2 rows in for
+  // the odd CTA); a narrower last tile receives the whole box, the MMA uses
+  // ncols.
+  template <bool PAIR>
   __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
-                       uint8_t* sB, uint64_t* bar) const {
-    tma_load_2d(sA, a, bar, kb * kBK, ui.a_row);
-    tma_load_2d(sB, ui.b_sel == 0 ? b : tmBv, bar, kb * kBK, ui.b_row);
+                       uint8_t* sB, uint32_t bar) const {
+    tma_load_2d_at<PAIR>(sA, a, bar, kb * kBK, ui.a_row);
+    tma_load_2d_at<PAIR>(sB, ui.b_sel == 0 ? b : tmBv, bar, kb * kBK, ui.b_row);
   }
   __device__ int num_units() const { return p.num_units; }
   // kind 0 = q, 1 = k, 2 = v
@@ -249,27 +323,28 @@ struct FwdSched {
     }
   }
   __device__ Unit unit(int u) const {
-    const int m = u / p.n_tiles, j = u % p.n_tiles;
+    const int j = u % p.n_tiles;
     int kind, head0, nh;
     decode(j, kind, head0, nh);
     Unit r;
-    r.a_row = m * kBM;
+    r.a_row = mtile(u) * kBM;
     if (kind == 0) {
       r.b_row = head0 * p.d_qk;
       r.ncols = nh * p.d_qk;
-      r.b_bytes = p.hq * p.d_qk * kBK;
+      r.b_bytes = p.hq * p.d_qk / pair * kBK;
       r.b_sel = 0;
     } else if (kind == 1) {
       r.b_row = p.H * p.d_qk + head0 * p.d_qk;
       r.ncols = nh * p.d_qk;
-      r.b_bytes = p.hq * p.d_qk * kBK;
+      r.b_bytes = p.hq * p.d_qk / pair * kBK;
       r.b_sel = 0;
     } else {
       r.b_row = 2 * p.H * p.d_qk + head0 * p.d_v;
       r.ncols = nh * p.d_v;
-      r.b_bytes = 2 * p.d_v * kBK;
+      r.b_bytes = 2 * p.d_v / pair * kBK;
       r.b_sel = 1;
     }
+    r.b_row += rank * (r.ncols / pair);
     r.kb0 = 0;
     r.kb1 = p.kblocks;
     return r;
@@ -294,7 +369,7 @@ struct FwdEpi {
   const float4* rope_row;   // entry j of this token: cos, cos, sin, sin of pairs 2j, 2j + 1
 
   __device__ void prepare(int u) {
-    const int m = u / p.n_tiles;
+    const int m = sc.mtile(u);
     sc.decode(u % p.n_tiles, kind, head0, nh);
     t = m * kBM + qw * 32 + lane;
     valid = t < p.T;
@@ -330,7 +405,7 @@ struct FwdEpi {
 
   __device__ void process(int u, uint32_t tacc) {
     constexpr int HALF = DQK / 2;
-    const int ty = (u / p.n_tiles) * kBM + qw * 32;
+    const int ty = sc.mtile(u) * kBM + qw * 32;
     for (int hh = sub; hh < nh; hh += nsub) {  // this warp's heads of the unit
       const int h = head0 + hh;
       uint8_t* buf = acquire();
@@ -378,7 +453,7 @@ struct FwdEpi {
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && ty < p.T) {   // (a pair's second tile may lie wholly past T)
           const CUtensorMap* map = kind == 0 ? tq : tk;
 #pragma unroll
           for (int b = 0; b < DQK / 32; ++b) tma_store_3d(map, buf + b * 2048, 32 * b, ty, h);
@@ -404,7 +479,7 @@ struct FwdEpi {
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && ty < p.T) {
 #pragma unroll
           for (int b = 0; b < 4; ++b) tma_store_3d(tv, buf + b * 2048, 32 * b, ty, h);
           bulk_commit();
@@ -418,16 +493,16 @@ struct FwdEpi {
 constexpr int kFwdEW = 8, kDxEW = 4, kDwEW = 8;
 constexpr int kFwdEPB = 8192, kDxEPB = 8192;
 
-template <int DQK>
+template <int DQK, bool PAIR>
 __global__ void __launch_bounds__(gemm_threads(kFwdEW), 1)
     fwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmBv,
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ FwdParams p, DevStatus st,
-                    int stages) {
-  FwdSched sc{p, &tmBv};
+                    Ring ring) {
+  FwdSched sc{p, &tmBv, PAIR ? static_cast<int>(cluster_rank()) : 0, PAIR ? 2 : 1};
   FwdEpi<DQK> epi{p, sc, &tq, &tk, &tv, st};
-  gemm_body<kFwdEW, kFwdEPB>(sc, epi, &tmA, &tmB, stages, st, KID_FWD_GEMM);
+  gemm_body<kFwdEW, kFwdEPB, PAIR>(sc, epi, &tmA, &tmB, ring, st, KID_FWD_GEMM);
 }
 
 // ---------------------------------------------------------------------------
@@ -436,17 +511,23 @@ __global__ void __launch_bounds__(gemm_threads(kFwdEW), 1)
 struct DxSched {
   static constexpr bool kMN = false;
   const DxParams& p;
+  int rank, pair;
+  __device__ int mtile(int u) const { return (u / p.n_tiles) * pair + rank; }
+  // A: 128 tokens of dY8; B: one box of bn / pair rows of W8T (this CTA's
+  // half of the tile's columns in a pair)
+  template <bool PAIR>
   __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
-                       uint8_t* sB, uint64_t* bar) const {
-    load_k_major(ui, kb, a, b, sA, sB, bar, p.bn);
+                       uint8_t* sB, uint32_t bar) const {
+    tma_load_2d_at<PAIR>(sA, a, bar, kb * kBK, ui.a_row);
+    tma_load_2d_at<PAIR>(sB, b, bar, kb * kBK, ui.b_row);
   }
   __device__ int num_units() const { return p.num_units; }
   __device__ Unit unit(int u) const {
     Unit r;
-    r.a_row = (u / p.n_tiles) * kBM;
-    r.b_row = (u % p.n_tiles) * p.bn;
+    r.a_row = mtile(u) * kBM;
+    r.b_row = (u % p.n_tiles) * p.bn + rank * (p.bn / pair);
     r.ncols = p.bn;
-    r.b_bytes = p.bn * kBK;
+    r.b_bytes = p.bn / pair * kBK;
     r.b_sel = 0;
     r.kb0 = 0;
     r.kb1 = p.kblocks;
@@ -456,10 +537,11 @@ struct DxSched {
 
 struct DxEpi {
   const DxParams& p;
+  const DxSched& sc;
   const CUtensorMap* tdx;
   uint8_t* stage;
   int qw, sub, nsub, lane, ring;
-  float sc;
+  float scl;   // s_dy * s_w
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t* stage_) {
     qw = qw_;
     sub = sub_;
@@ -467,7 +549,7 @@ struct DxEpi {
     lane = lane_;
     stage = stage_;
     ring = 0;
-    sc = (*p.dy_scale) * (*p.w_scale);
+    scl = (*p.dy_scale) * (*p.w_scale);
   }
   __device__ void finish() {
     if (lane == 0) bulk_wait_all<0>();
@@ -475,7 +557,7 @@ struct DxEpi {
   }
   __device__ void prepare(int) {}
   __device__ void process(int u, uint32_t tacc) {
-    const int m = u / p.n_tiles, j = u % p.n_tiles;
+    const int m = sc.mtile(u), j = u % p.n_tiles;
     const int ty = m * kBM + qw * 32;
     const int share = p.bn / nsub;   // this warp's columns: [sub * share, (sub + 1) * share)
     for (int c0 = sub * share; c0 < (sub + 1) * share; c0 += 32) {
@@ -491,12 +573,13 @@ struct DxEpi {
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(raw[g * 16 + 2 * i]) * sc, __uint_as_float(raw[g * 16 + 2 * i + 1]) * sc);
+          w[i] = pack_bf16x2(__uint_as_float(raw[g * 16 + 2 * i]) * scl,
+                             __uint_as_float(raw[g * 16 + 2 * i + 1]) * scl);
         stage16(slot, lane, g * 16, w);
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && ty < p.T) {   // (a pair's second tile may lie wholly past T)
         tma_store_2d(tdx, slot, j * p.bn + c0, ty);
         bulk_commit();
       }
@@ -505,13 +588,14 @@ struct DxEpi {
   }
 };
 
+template <bool PAIR>
 __global__ void __launch_bounds__(gemm_threads(kDxEW), 1)
     dx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tdx, const __grid_constant__ DxParams p, DevStatus st,
-                   int stages) {
-  DxSched sc{p};
-  DxEpi epi{p, &tdx};
-  gemm_body<kDxEW, kDxEPB>(sc, epi, &tmA, &tmB, stages, st, KID_DX_GEMM);
+                   Ring ring) {
+  DxSched sc{p, PAIR ? static_cast<int>(cluster_rank()) : 0, PAIR ? 2 : 1};
+  DxEpi epi{p, sc, &tdx};
+  gemm_body<kDxEW, kDxEPB, PAIR>(sc, epi, &tmA, &tmB, ring, st, KID_DX_GEMM);
 }
 
 // ---------------------------------------------------------------------------
@@ -524,22 +608,29 @@ __global__ void __launch_bounds__(gemm_threads(kDxEW), 1)
 struct DwSched {
   static constexpr bool kMN = true;
   const DwParams& p;
-  // A: one box of 128 tokens x 128 packed columns at (a_row, k); B: ncols/128
-  // boxes of 128 tokens x 128 model columns at (b_row + 128 j, k).
+  int rank, pair;
+  // units: split-major over (pairs of) 128-row tiles of dW and bn-column tiles
+  __device__ int tiles_per_split() const { return (p.m_tiles + pair - 1) / pair * p.n_tiles; }
+  __device__ int split_of(int u) const { return u / tiles_per_split(); }
+  __device__ int mtile(int u) const { return (u % tiles_per_split()) / p.n_tiles * pair + rank; }
+  __device__ int ntile(int u) const { return (u % tiles_per_split()) % p.n_tiles; }
+  // A: one box of 128 tokens x 128 packed columns at (a_row, k); B: this
+  // CTA's bn / pair model columns as boxes of 128 tokens x 128 columns.
+  template <bool PAIR>
   __device__ void load(const Unit& ui, int kb, const CUtensorMap* a, const CUtensorMap* b, uint8_t* sA,
-                       uint8_t* sB, uint64_t* bar) const {
-    tma_load_2d(sA, a, bar, ui.a_row, kb * kBK);
-    for (int j = 0; j < ui.ncols / 128; ++j) tma_load_2d(sB + j * 16384, b, bar, ui.b_row + 128 * j, kb * kBK);
+                       uint8_t* sB, uint32_t bar) const {
+    tma_load_2d_at<PAIR>(sA, a, bar, ui.a_row, kb * kBK);
+    for (int j = 0; j < ui.ncols / pair / 128; ++j)
+      tma_load_2d_at<PAIR>(sB + j * 16384, b, bar, ui.b_row + 128 * j, kb * kBK);
   }
   __device__ int num_units() const { return p.num_units; }
   __device__ Unit unit(int u) const {
-    const int mn = p.m_tiles * p.n_tiles;
-    const int tile = u % mn, split = u / mn;
+    const int split = split_of(u);
     Unit r;
-    r.a_row = (tile / p.n_tiles) * kBM;
-    r.b_row = (tile % p.n_tiles) * p.bn;
+    r.a_row = mtile(u) * kBM;
+    r.b_row = ntile(u) * p.bn + rank * (p.bn / pair);
     r.ncols = p.bn;
-    r.b_bytes = p.bn * kBK;
+    r.b_bytes = p.bn / pair * kBK;
     r.b_sel = 0;
     r.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks_total / p.splits);
     r.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks_total / p.splits);
@@ -549,6 +640,7 @@ struct DwSched {
 
 struct DwEpi {
   const DwParams& p;
+  const DwSched& sc;
   int qw, sub, nsub, lane;
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t*) {
     qw = qw_;
@@ -559,8 +651,12 @@ struct DwEpi {
   __device__ void finish() {}
   __device__ void prepare(int) {}
   __device__ void process(int u, uint32_t tacc) {
-    // unit u owns partials[u][bn][128] (column-major tile): coalesced stores
-    float* dst = p.partials + static_cast<int64_t>(u) * p.bn * kBM + qw * 32 + lane;
+    // tile (split, m, n) owns partials[split][m][n][bn][128] (column-major):
+    // coalesced stores; the odd CTA of the last pair may lie past the rows
+    const int m = sc.mtile(u);
+    if (m >= p.m_tiles) return;
+    const int64_t tile = (static_cast<int64_t>(sc.split_of(u)) * p.m_tiles + m) * p.n_tiles + sc.ntile(u);
+    float* dst = p.partials + tile * p.bn * kBM + qw * 32 + lane;
     const int share = p.bn / nsub;
     for (int c0 = sub * share; c0 < (sub + 1) * share; c0 += 32) {
       uint32_t raw[32];
@@ -573,12 +669,13 @@ struct DwEpi {
   }
 };
 
+template <bool PAIR>
 __global__ void __launch_bounds__(gemm_threads(kDwEW), 1)
     dw_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ DwParams p, DevStatus st, int stages) {
-  DwSched sc{p};
-  DwEpi epi{p};
-  gemm_body<kDwEW, 0>(sc, epi, &tmA, &tmB, stages, st, KID_DW_GEMM);
+                   const __grid_constant__ DwParams p, DevStatus st, Ring ring) {
+  DwSched sc{p, PAIR ? static_cast<int>(cluster_rank()) : 0, PAIR ? 2 : 1};
+  DwEpi epi{p, sc};
+  gemm_body<kDwEW, 0, PAIR>(sc, epi, &tmA, &tmB, ring, st, KID_DW_GEMM);
 }
 
 // dW[n][d] = bf16(s_dy * s_x * sum over splits, in split order, of the
@@ -615,61 +712,130 @@ __global__ void __launch_bounds__(128) dw_reduce_kernel(const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
-constexpr int kFwdStages = 3, kDxStages = 4, kDwStages = 4;
-
+// Every GEMM kernel may use up to kSmemMax bytes of dynamic shared memory.
 template <class K>
-static cudaError_t set_smem_once(K kernel, int bytes, bool (&done)[64]) {
+static cudaError_t set_smem_once(K kernel, bool (&done)[64]) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
   if (e == cudaSuccess && dev < 64) done[dev] = true;
   return e;
 }
 
-template <int DQK>
-static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
-                                const CUtensorMap& tq,
-                                const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int grid,
-                                DevStatus st, cudaStream_t s) {
-  static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kFwdStages, kFwdEW, kFwdEPB);
-  cudaError_t e = set_smem_once(fwd_gemm_kernel<DQK>, smem, done);
-  if (e != cudaSuccess) return e;
-  fwd_gemm_kernel<DQK><<<grid, gemm_threads(kFwdEW), smem, s>>>(tmA, tmB, tmBv, tq, tk, tv, p, st, kFwdStages);
-  return cudaGetLastError();
+// Co-resident 2-CTA clusters of a kernel at a given shared-memory size,
+// queried once per (kernel, device, size).
+struct ClusterCache {
+  int smem[64] = {};
+  int clusters[64] = {};
+};
+
+// Persistent launch: one CTA per SM (at most one per unit), or for pairs one
+// 2-CTA cluster per co-resident pair of SMs (at most one per unit).
+template <class... KArgs, class... Args>
+static cudaError_t launch_persistent(void (*kernel)(KArgs...), bool pair, int units, int sms, int threads, int smem,
+                                     ClusterCache& cache, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  int grid = units < sms ? units : sms;
+  if (pair) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int clusters = dev < 64 && cache.smem[dev] == smem ? cache.clusters[dev] : 0;
+    if (clusters <= 0) {
+      cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1));
+      e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (clusters <= 0) return cudaErrorInvalidConfiguration;
+      if (dev < 64) {
+        cache.smem[dev] = smem;
+        cache.clusters[dev] = clusters;
+      }
+    }
+    grid = 2 * (units < clusters ? units : clusters);
+  }
+  cfg.gridDim = dim3(grid);
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
-                            const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                            int grid, DevStatus st, cudaStream_t s) {
+template <int DQK, bool PAIR>
+static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
+                                const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                                int sms, DevStatus st, cudaStream_t s) {
+  static bool done[64] = {};
+  static ClusterCache cache;
+  // B tiles: hq heads of q or k, or two heads of v (this CTA's half in a pair)
+  const int brows = (p.hq * DQK > 2 * p.d_v ? p.hq * DQK : 2 * p.d_v) / p.pair;
+  const Ring ring = ring_for(brows * kBK, kFwdEW, kFwdEPB);
+  cudaError_t e = set_smem_once(fwd_gemm_kernel<DQK, PAIR>, done);
+  if (e != cudaSuccess) return e;
+  return launch_persistent(fwd_gemm_kernel<DQK, PAIR>, PAIR, p.num_units, sms, gemm_threads(kFwdEW),
+                           gemm_smem_bytes(ring, kFwdEW, kFwdEPB), cache, s, tmA, tmB, tmBv, tq, tk, tv, p, st,
+                           ring);
+}
+
+template <bool PAIR>
+static cudaError_t launch_fwd_p(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
+                                const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                                int sms, DevStatus st, cudaStream_t s) {
   switch (p.d_qk) {
-    case 64: return launch_fwd_t<64>(tmA, tmB, tmBv, tq, tk, tv, p, grid, st, s);
-    case 96: return launch_fwd_t<96>(tmA, tmB, tmBv, tq, tk, tv, p, grid, st, s);
-    case 128: return launch_fwd_t<128>(tmA, tmB, tmBv, tq, tk, tv, p, grid, st, s);
+    case 64: return launch_fwd_t<64, PAIR>(tmA, tmB, tmBv, tq, tk, tv, p, sms, st, s);
+    case 96: return launch_fwd_t<96, PAIR>(tmA, tmB, tmBv, tq, tk, tv, p, sms, st, s);
+    case 128: return launch_fwd_t<128, PAIR>(tmA, tmB, tmBv, tq, tk, tv, p, sms, st, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
-                           const DxParams& p, int grid, DevStatus st, cudaStream_t s) {
-  static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kDxStages, kDxEW, kDxEPB);
-  cudaError_t e = set_smem_once(dx_gemm_kernel, smem, done);
-  if (e != cudaSuccess) return e;
-  dx_gemm_kernel<<<grid, gemm_threads(kDxEW), smem, s>>>(tmA, tmB, tdx, p, st, kDxStages);
-  return cudaGetLastError();
+cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
+                            const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                            int sms, DevStatus st, cudaStream_t s) {
+  return p.pair == 2 ? launch_fwd_p<true>(tmA, tmB, tmBv, tq, tk, tv, p, sms, st, s)
+                     : launch_fwd_p<false>(tmA, tmB, tmBv, tq, tk, tv, p, sms, st, s);
 }
 
-cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int grid,
-                           DevStatus st, cudaStream_t s) {
+template <bool PAIR>
+static cudaError_t launch_dx_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
+                               const DxParams& p, int sms, DevStatus st, cudaStream_t s) {
   static bool done[64] = {};
-  const int smem = gemm_smem_bytes(kDwStages, kDwEW, 0);
-  cudaError_t e = set_smem_once(dw_gemm_kernel, smem, done);
+  static ClusterCache cache;
+  const Ring ring = ring_for(p.bn / p.pair * kBK, kDxEW, kDxEPB);
+  cudaError_t e = set_smem_once(dx_gemm_kernel<PAIR>, done);
   if (e != cudaSuccess) return e;
-  dw_gemm_kernel<<<grid, gemm_threads(kDwEW), smem, s>>>(tmA, tmB, p, st, kDwStages);
-  return cudaGetLastError();
+  return launch_persistent(dx_gemm_kernel<PAIR>, PAIR, p.num_units, sms, gemm_threads(kDxEW),
+                           gemm_smem_bytes(ring, kDxEW, kDxEPB), cache, s, tmA, tmB, tdx, p, st, ring);
+}
+
+cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
+                           const DxParams& p, int sms, DevStatus st, cudaStream_t s) {
+  return p.pair == 2 ? launch_dx_t<true>(tmA, tmB, tdx, p, sms, st, s) : launch_dx_t<false>(tmA, tmB, tdx, p, sms, st, s);
+}
+
+template <bool PAIR>
+static cudaError_t launch_dw_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,
+                               DevStatus st, cudaStream_t s) {
+  static bool done[64] = {};
+  static ClusterCache cache;
+  const Ring ring = ring_for(p.bn / p.pair * kBK, kDwEW, 0);
+  cudaError_t e = set_smem_once(dw_gemm_kernel<PAIR>, done);
+  if (e != cudaSuccess) return e;
+  return launch_persistent(dw_gemm_kernel<PAIR>, PAIR, p.num_units, sms, gemm_threads(kDwEW),
+                           gemm_smem_bytes(ring, kDwEW, 0), cache, s, tmA, tmB, p, st, ring);
+}
+
+cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,
+                           DevStatus st, cudaStream_t s) {
+  return p.pair == 2 ? launch_dw_t<true>(tmA, tmB, p, sms, st, s) : launch_dw_t<false>(tmA, tmB, p, sms, st, s);
 }
 
 cudaError_t launch_dw_reduce(const DwParams& p, const float* dy_scale, const float* x_scale, uint16_t* dW,

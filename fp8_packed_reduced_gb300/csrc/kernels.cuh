@@ -38,7 +38,9 @@ cudaError_t launch_rope_table(float* table, int max_pos, int d_qk, double base, 
 cudaError_t launch_selftest_wait(DevStatus st, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
-// GEMMs (tcgen05, M = 128 tiles, K-major E4M3 operands via TMA)
+// GEMMs (tcgen05, E4M3 operands via TMA).  With pair = 2 a unit is a 256-row
+// tile computed by a 2-CTA cluster (one MMA per K step over both CTAs'
+// shared memory); with pair = 1 a 128-row tile computed by one CTA.
 // ---------------------------------------------------------------------------
 struct FwdParams {
   int T, H, d_qk, d_v;
@@ -46,7 +48,8 @@ struct FwdParams {
   int nq;            // Q tiles (= K tiles) per 128-token block
   int nv;            // V tiles per block (2 heads each)
   int n_tiles;       // 2*nq + nv
-  int num_units;     // ceil(T/128) * n_tiles
+  int pair;          // CTAs per unit (1 or 2)
+  int num_units;     // ceil(ceil(T/128) / pair) * n_tiles
   int kblocks;       // D / 128
   float eps;
   const float* x_scale;
@@ -58,23 +61,26 @@ struct FwdParams {
 };
 
 struct DxParams {
-  int T, D, bn, n_tiles, num_units, kblocks;
+  int T, D, bn, n_tiles, pair, num_units, kblocks;   // num_units = ceil(ceil(T/128) / pair) * n_tiles
   const float* dy_scale;
   const float* w_scale;
 };
 
 struct DwParams {
-  int N, D, bn, m_tiles, n_tiles, splits, num_units, kblocks_total;   // kblocks_total = ceil(T/128)
+  // num_units = splits * ceil(m_tiles / pair) * n_tiles; kblocks_total = ceil(T/128)
+  int N, D, bn, m_tiles, n_tiles, pair, splits, num_units, kblocks_total;
   float* partials;    // [splits][m_tiles][n_tiles][bn][128] float32
 };
 
-// tmB / tmBv: W8 with box heights hq*d_qk (q/k tiles) and 2*d_v (v tiles).
+// Persistent launches sized to the device (`sms` multiprocessors).
+// tmB / tmBv: W8 with box heights hq*d_qk/pair (q/k tiles) and 2*d_v/pair (v
+// tiles); dX: W8T with box height bn/pair.
 cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
                             const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                            int grid, DevStatus st, cudaStream_t s);
+                            int sms, DevStatus st, cudaStream_t s);
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
-                           const DxParams& p, int grid, DevStatus st, cudaStream_t s);
-cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int grid,
+                           const DxParams& p, int sms, DevStatus st, cudaStream_t s);
+cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,
                            DevStatus st, cudaStream_t s);
 cudaError_t launch_dw_reduce(const DwParams& p, const float* dy_scale, const float* x_scale, uint16_t* dW,
                              cudaStream_t s);

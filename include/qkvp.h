@@ -211,6 +211,17 @@ int qkvp_set_timing_events(void* const* events, int n);
 /* Number of events recorded since the last qkvp_set_timing_events. */
 int qkvp_timing_events_recorded(void);
 
+/* GEMM tiling: which of the three GEMMs run on CTA pairs.  Bit 0 = forward,
+ * bit 1 = dX, bit 2 = dW.  A paired GEMM computes each 256-row accumulator
+ * tile with one tcgen05 MMA over two SMs (a 2-CTA cluster, cta_group::2):
+ * each SM loads its own 128 rows of A and half of B, so the shared-memory and
+ * L2 traffic of B per SM is halved.  Results are the same either way (every
+ * output element is the same fp32 sum over K in the same order).  The dW GEMM
+ * is paired only when D is a multiple of 256.  Returns the previous mask, or
+ * -1 (mask unchanged) for a mask outside 0..7.  Process-wide, not
+ * thread-safe; meant for tests and tuning.  Default 6 (dX and dW paired). */
+int qkvp_set_cta_pairs(int mask);
+
 #ifdef __cplusplus
 }
 #endif

@@ -119,6 +119,10 @@ def test_other_validation_codes(qk):
     assert lib.qkvp_set_wait_timeout_ns(10) == qk.ERR_INVALID_ARGUMENT
     assert lib.qkvp_set_wait_timeout_ns(2_000_000_000) == qk.OK
     assert lib.qkvp_workspace_init(None, 256, None) == qk.ERR_INVALID_ARGUMENT
+    prev = lib.qkvp_set_cta_pairs(3)
+    assert 0 <= prev <= 7
+    assert lib.qkvp_set_cta_pairs(8) == -1 and lib.qkvp_set_cta_pairs(-1) == -1
+    assert lib.qkvp_set_cta_pairs(prev) == 3
 
 
 def test_product_path_refuses_without_library(tmp_path, monkeypatch):

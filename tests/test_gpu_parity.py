@@ -107,8 +107,7 @@ def test_bank_other_shapes(qk, H, D, dqk):
 # Forward
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("s", SHAPES, ids=IDS)
-def test_forward_matches_oracle(qk, s):
+def _check_forward(qk, s):
     r = _run_forward(qk, s)
     inp = r["inp"]
     fw = oracle.forward(f32(inp["x"]), r["oW8"], r["os_w"], inp["pos"].numpy(), s.H, s.d_qk, s.d_v)
@@ -117,6 +116,11 @@ def test_forward_matches_oracle(qk, s):
     for name in ("q", "k", "v"):
         assert_close(f32(r[name]), fw[name], name)
     assert_close(r["saved"].rstd.cpu().numpy(), fw["rstd"], "rstd")
+
+
+@pytest.mark.parametrize("s", SHAPES, ids=IDS)
+def test_forward_matches_oracle(qk, s):
+    _check_forward(qk, s)
 
 
 def test_forward_deterministic(qk):
@@ -152,8 +156,7 @@ def _run_backward(qk, s, seed=0):
     return out, bw, r, fw
 
 
-@pytest.mark.parametrize("s", SHAPES, ids=IDS)
-def test_backward_matches_oracle(qk, s):
+def _check_backward(qk, s):
     out, bw, r, fw = _run_backward(qk, s)
     dy_scale = out["dy_scale"].item()
     assert abs(dy_scale - float(bw["dy_scale"])) <= 1e-6 * float(bw["dy_scale"])
@@ -171,6 +174,27 @@ def test_backward_matches_oracle(qk, s):
     if np.array_equal(dY8, bw["dY8"]):
         assert_close(f32(out["dx"]), bw["dX"], "dx")
         assert_close(f32(out["dW"]), bw["dW"], "dW", bf16_rounding=rank_one)
+
+
+@pytest.mark.parametrize("s", SHAPES, ids=IDS)
+def test_backward_matches_oracle(qk, s):
+    _check_backward(qk, s)
+
+
+# The GEMMs on one CTA per tile (the default runs them on 2-CTA clusters):
+# every mask must give the oracle's results.
+PAIR_SHAPES = [SHAPES[0], SHAPES[1], SHAPES[2], SHAPES[3], SHAPES[6]]
+
+
+@pytest.mark.parametrize("mask", [0, 5, 2])
+@pytest.mark.parametrize("s", PAIR_SHAPES, ids=[f"T{s.T}_D{s.D}_H{s.H}_dqk{s.d_qk}" for s in PAIR_SHAPES])
+def test_cta_pair_masks_match_oracle(qk, s, mask):
+    prev = qk.set_cta_pairs(mask)
+    try:
+        _check_forward(qk, s)
+        _check_backward(qk, s)
+    finally:
+        qk.set_cta_pairs(prev)
 
 
 def test_gradient_gemms_on_the_same_codes(qk):

@@ -88,7 +88,8 @@ int check_dims(const qkvp_dims* d) {
   return QKVP_OK;
 }
 
-// Workspace: [status 256 B][x amax partials][dY amax partials][dW partials]
+// Workspace: [status 256 B][x amax partials][dY amax partials][dW tile
+// counters][dW partials]
 constexpr size_t kStatusBytes = 256;
 constexpr int kMaxParts = 4096;
 constexpr size_t kPartsBytes = kMaxParts * sizeof(float);
@@ -109,8 +110,13 @@ DwShape dw_shape(const qkvp_dims* d) {
 size_t dw_partial_bytes(const DwShape& s, int splits) {
   return static_cast<size_t>(splits) * s.m_tiles * s.n_tiles * s.bn * 128 * sizeof(float);
 }
+// one counter per (tile, dW epilogue warp), padded to 256 bytes
+size_t dw_counter_bytes(const DwShape& s) {
+  return (static_cast<size_t>(s.m_tiles) * s.n_tiles * kDwEpiWarps * sizeof(int) + 255) / 256 * 256;
+}
 size_t ws_bytes_for(const qkvp_dims* d) {
-  return kStatusBytes + 2 * kPartsBytes + dw_partial_bytes(dw_shape(d), kMaxSplits);
+  const DwShape s = dw_shape(d);
+  return kStatusBytes + 2 * kPartsBytes + dw_counter_bytes(s) + dw_partial_bytes(s, kMaxSplits);
 }
 
 // Split count for the dW GEMM: the fewest splits whose units fill the
@@ -377,7 +383,8 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* dyparts = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
-  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes);
+  int* dwcount = reinterpret_cast<int*>(wsb + kStatusBytes + 2 * kPartsBytes);
+  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes + dw_counter_bytes(dw_shape(dims)));
   const DevStatus st = dev_status(ws);
 
   BwdMaps m;
@@ -446,9 +453,11 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   wp.splits = choose_splits(pair_tiles, ds.kblocks_total, sms / wp.pair);
   wp.num_units = wp.splits * pair_tiles;
   wp.partials = dwparts;
+  wp.counters = dwcount;
+  wp.dy_scale = dy_scale;
+  wp.x_scale = x_scale;
+  wp.dW = dW;
   QKVP_TRY_CUDA(launch_dw_gemm(tm_dy, tm_x8, wp, sms, st, s));
-  mark(s);
-  QKVP_TRY_CUDA(launch_dw_reduce(wp, dy_scale, x_scale, dW, s));
   mark(s);
   return QKVP_OK;
 }

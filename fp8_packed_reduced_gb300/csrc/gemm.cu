@@ -260,6 +260,7 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
         else
           mbar_arrive(&g.tempty[buf]);
       }
+      epi.post(u);   // work after the accumulator buffer is released
     }
     epi.finish();
   }
@@ -368,6 +369,7 @@ struct FwdEpi {
   bool valid;
   const float4* rope_row;   // entry j of this token: cos, cos, sin, sin of pairs 2j, 2j + 1
 
+  __device__ void post(int) {}
   __device__ void prepare(int u) {
     const int m = sc.mtile(u);
     sc.decode(u % p.n_tiles, kind, head0, nh);
@@ -490,7 +492,7 @@ struct FwdEpi {
 };
 
 // Epilogue warps and per-warp staging bytes of each GEMM.
-constexpr int kFwdEW = 8, kDxEW = 4, kDwEW = 8;
+constexpr int kFwdEW = 8, kDxEW = 4, kDwEW = kDwEpiWarps;
 constexpr int kFwdEPB = 8192, kDxEPB = 8192;
 
 template <int DQK, bool PAIR>
@@ -556,6 +558,7 @@ struct DxEpi {
     __syncwarp();
   }
   __device__ void prepare(int) {}
+  __device__ void post(int) {}
   __device__ void process(int u, uint32_t tacc) {
     const int m = sc.mtile(u), j = u % p.n_tiles;
     const int ty = m * kBM + qw * 32;
@@ -638,25 +641,42 @@ struct DwSched {
   }
 };
 
+// Epilogue of the dW GEMM.  Each unit stores its fp32 partial tile in the
+// layout [bn / 4][128 rows][4 columns], so that both the stores here and the
+// loads of the reduction are 16 bytes per lane and coalesced.  An epilogue
+// warp owns the same sub-tile (32 rows x bn / nsub columns) of every split of
+// a tile, and counts itself on that sub-tile's counter once its part of the
+// partial is stored; the warp that completes the count (the last split to
+// finish, in whatever order they finish) then sums the sub-tile's partials
+// over all splits in split order (the same sum, bit for bit, whichever warp
+// does it), scales by s_dy * s_x, writes it to dW in bf16 and resets the
+// counter for the next call.  No barrier spans warps, so a warp that leaves
+// early on an expired wait stalls no other.
 struct DwEpi {
   const DwParams& p;
   const DwSched& sc;
-  int qw, sub, nsub, lane;
+  int qw, sub, nsub, lane, ew;
+  bool last;   // this warp completed its sub-tile of the unit just processed
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t*) {
     qw = qw_;
     sub = sub_;
     nsub = nsub_;
     lane = lane_;
+    ew = qw + 4 * sub;
   }
   __device__ void finish() {}
   __device__ void prepare(int) {}
+  __device__ int64_t tile_of(int u, int split) const {
+    return (static_cast<int64_t>(split) * p.m_tiles + sc.mtile(u)) * p.n_tiles + sc.ntile(u);
+  }
+  // float4 index of columns [c, c + 4) of row `row` inside a partial tile
+  __device__ static int quad(int c, int row) { return (c >> 2) * kBM + row; }
   __device__ void process(int u, uint32_t tacc) {
-    // tile (split, m, n) owns partials[split][m][n][bn][128] (column-major):
-    // coalesced stores; the odd CTA of the last pair may lie past the rows
-    const int m = sc.mtile(u);
-    if (m >= p.m_tiles) return;
-    const int64_t tile = (static_cast<int64_t>(sc.split_of(u)) * p.m_tiles + m) * p.n_tiles + sc.ntile(u);
-    float* dst = p.partials + tile * p.bn * kBM + qw * 32 + lane;
+    last = false;
+    // the odd CTA of the last pair may lie past the rows
+    if (sc.mtile(u) >= p.m_tiles) return;
+    const int row = qw * 32 + lane;
+    float4* dst = reinterpret_cast<float4*>(p.partials + tile_of(u, sc.split_of(u)) * p.bn * kBM);
     const int share = p.bn / nsub;
     for (int c0 = sub * share; c0 < (sub + 1) * share; c0 += 32) {
       uint32_t raw[32];
@@ -664,8 +684,62 @@ struct DwEpi {
       tmem_ld16(tacc + c0 + 16, raw + 16);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) dst[static_cast<int64_t>(c0 + i) * kBM] = __uint_as_float(raw[i]);
+      for (int i = 0; i < 8; ++i)
+        dst[quad(c0 + 4 * i, row)] = make_float4(__uint_as_float(raw[4 * i]), __uint_as_float(raw[4 * i + 1]),
+                                                 __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3]));
     }
+    __threadfence();   // this lane's stores are visible device-wide before the count
+    __syncwarp();
+    int old = 0;
+    if (lane == 0) old = atomicAdd(p.counters + (sc.mtile(u) * p.n_tiles + sc.ntile(u)) * kDwEW + ew, 1);
+    last = __shfl_sync(0xffffffffu, old, 0) == p.splits - 1;
+  }
+  __device__ void post(int u) {
+    if (!last) return;
+    __threadfence();
+    constexpr int QB = 4;   // column quads per batch
+    constexpr int SB = 4;   // splits per batch (their loads are all in flight together)
+    const int m = sc.mtile(u), nt = sc.ntile(u);
+    const int row = qw * 32 + lane, n = m * kBM + row;
+    const float scl = (*p.dy_scale) * (*p.x_scale);
+    const int share = p.bn / nsub;
+    const float4* src = reinterpret_cast<const float4*>(p.partials + tile_of(u, 0) * p.bn * kBM);
+    const int64_t split_stride = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.bn * kBM / 4;   // float4s
+    for (int c0 = sub * share; c0 < (sub + 1) * share; c0 += 4 * QB) {
+      float4 acc[QB];
+#pragma unroll
+      for (int q = 0; q < QB; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < p.splits; s0 += SB) {   // split order: the same sum on every run
+        float4 v[SB][QB];
+#pragma unroll
+        for (int j = 0; j < SB; ++j)
+          if (s0 + j < p.splits)
+#pragma unroll
+            for (int q = 0; q < QB; ++q) v[j][q] = __ldcg(src + (s0 + j) * split_stride + quad(c0 + 4 * q, row));
+#pragma unroll
+        for (int j = 0; j < SB; ++j)
+          if (s0 + j < p.splits)
+#pragma unroll
+            for (int q = 0; q < QB; ++q) {
+              acc[q].x += v[j][q].x;
+              acc[q].y += v[j][q].y;
+              acc[q].z += v[j][q].z;
+              acc[q].w += v[j][q].w;
+            }
+      }
+      if (n < p.N) {
+        uint32_t w[2 * QB];
+#pragma unroll
+        for (int q = 0; q < QB; ++q) {
+          w[2 * q] = pack_bf16x2(acc[q].x * scl, acc[q].y * scl);
+          w[2 * q + 1] = pack_bf16x2(acc[q].z * scl, acc[q].w * scl);
+        }
+        uint4* out = reinterpret_cast<uint4*>(p.dW + static_cast<int64_t>(n) * p.D + nt * p.bn + c0);
+        out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    if (lane == 0) p.counters[(m * p.n_tiles + nt) * kDwEW + ew] = 0;   // every split has counted
   }
 };
 
@@ -676,37 +750,6 @@ __global__ void __launch_bounds__(gemm_threads(kDwEW), 1)
   DwSched sc{p, PAIR ? static_cast<int>(cluster_rank()) : 0, PAIR ? 2 : 1};
   DwEpi epi{p, sc};
   gemm_body<kDwEW, 0, PAIR>(sc, epi, &tmA, &tmB, ring, st, KID_DW_GEMM);
-}
-
-// dW[n][d] = bf16(s_dy * s_x * sum over splits, in split order, of the
-// partials).  One thread per (row, 4 columns): all of its splits' loads are
-// issued before the first add.  grid: (m_tiles * n_tiles, bn / 4), 128 threads.
-constexpr int kMaxReduceSplits = 16;
-__global__ void __launch_bounds__(128) dw_reduce_kernel(const __grid_constant__ DwParams p, const float* dy_scale,
-                                                        const float* x_scale, uint16_t* dW) {
-  const int tile = blockIdx.x, c0 = blockIdx.y * 4;
-  const int row = threadIdx.x;
-  const int mn = p.m_tiles * p.n_tiles;
-  float v[kMaxReduceSplits][4];
-#pragma unroll
-  for (int s = 0; s < kMaxReduceSplits; ++s)
-    if (s < p.splits) {
-      const float* src = p.partials + (static_cast<int64_t>(s * mn + tile) * p.bn + c0) * kBM + row;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[s][i] = __ldcs(src + i * kBM);
-    }
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int s = 0; s < kMaxReduceSplits; ++s)
-    if (s < p.splits)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] += v[s][i];
-  const int n = (tile / p.n_tiles) * kBM + row;
-  if (n >= p.N) return;
-  const int d = (tile % p.n_tiles) * p.bn + c0;
-  const float sc = (*dy_scale) * (*x_scale);
-  *reinterpret_cast<uint2*>(dW + static_cast<int64_t>(n) * p.D + d) =
-      make_uint2(pack_bf16x2(acc[0] * sc, acc[1] * sc), pack_bf16x2(acc[2] * sc, acc[3] * sc));
 }
 
 // ---------------------------------------------------------------------------
@@ -836,13 +879,6 @@ static cudaError_t launch_dw_t(const CUtensorMap& tmA, const CUtensorMap& tmB, c
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,
                            DevStatus st, cudaStream_t s) {
   return p.pair == 2 ? launch_dw_t<true>(tmA, tmB, p, sms, st, s) : launch_dw_t<false>(tmA, tmB, p, sms, st, s);
-}
-
-cudaError_t launch_dw_reduce(const DwParams& p, const float* dy_scale, const float* x_scale, uint16_t* dW,
-                             cudaStream_t s) {
-  if (p.splits > kMaxReduceSplits) return cudaErrorInvalidValue;
-  dw_reduce_kernel<<<dim3(p.m_tiles * p.n_tiles, p.bn / 4), 128, 0, s>>>(p, dy_scale, x_scale, dW);
-  return cudaGetLastError();
 }
 
 }  // namespace qkvp

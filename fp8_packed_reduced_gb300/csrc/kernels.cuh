@@ -66,10 +66,17 @@ struct DxParams {
   const float* w_scale;
 };
 
+// Epilogue warps of the dW GEMM; each owns one counter per output tile.
+constexpr int kDwEpiWarps = 8;
+
 struct DwParams {
   // num_units = splits * ceil(m_tiles / pair) * n_tiles; kblocks_total = ceil(T/128)
   int N, D, bn, m_tiles, n_tiles, pair, splits, num_units, kblocks_total;
-  float* partials;    // [splits][m_tiles][n_tiles][bn][128] float32
+  float* partials;    // [splits][m_tiles][n_tiles] tiles of [bn / 4][128][4] float32
+  int* counters;      // [m_tiles * n_tiles * kDwEpiWarps] splits finished per sub-tile; 0 between calls
+  const float* dy_scale;
+  const float* x_scale;
+  uint16_t* dW;       // [N, D] bf16
 };
 
 // Persistent launches sized to the device (`sms` multiprocessors).
@@ -82,8 +89,7 @@ cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            const DxParams& p, int sms, DevStatus st, cudaStream_t s);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,
                            DevStatus st, cudaStream_t s);
-cudaError_t launch_dw_reduce(const DwParams& p, const float* dy_scale, const float* x_scale, uint16_t* dW,
-                             cudaStream_t s);
+
 
 // ---------------------------------------------------------------------------
 // Backward epilogue (norm/RoPE backward, dY amax, dY quantisation)

@@ -71,15 +71,19 @@ const char* qkvp_status_string(int status);
 
 /* Bytes of scratch that qkvp_forward and qkvp_backward need for `dims`
  * (one workspace serves both).  0 if dims are unsupported.  The workspace
- * starts with the device status word; zero it once with
- * qkvp_workspace_init before first use. */
+ * starts with the device status word and holds the dW GEMM's per-tile
+ * completion counters, which every backward leaves at zero; zero it once
+ * with qkvp_workspace_init before first use, and again after a device error
+ * (a call that stopped early may leave counters set).  Calls sharing one
+ * workspace must not overlap on the GPU. */
 size_t qkvp_workspace_bytes(const qkvp_dims* dims);
 
 /* Bytes of scratch that qkvp_quantize_bank needs for L layers (0 if the
  * shape is unsupported). */
 size_t qkvp_bank_workspace_bytes(int L, int D, int H, int d_qk, int d_v);
 
-/* Zero a workspace (status word and all partial buffers).  ws: device. */
+/* Zero a workspace (status word, counters and all partial buffers).
+ * ws: device. */
 int qkvp_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Read and clear the device status word at the start of `ws`.  Synchronises
@@ -167,7 +171,9 @@ int qkvp_forward(const qkvp_dims* dims, float eps,
  * dY_q = rstd * RoPE^T(dq - q * mean(dq * q)) (the same for k), dY_v = dv;
  * dY is quantised with its own scale into dY8, then
  *   dx = (dY8 . W8) * s_dy * s_w   with the cached W8T as the K-major operand
- *   dW = (dY8^T . x8) * s_dy * s_x with dY8 and x8 read as MN-major operands
+ *   dW = (dY8^T . x8) * s_dy * s_x with dY8 and x8 read as MN-major operands,
+ *        split over tokens; the split partials (fp32, in ws) are summed in
+ *        split order by the GEMM itself, so dW is the same on every run
  *   dq, dk    in  [H, T, d_qk] bf16     dv in [H, T, d_v] bf16
  *   q, k      in  [H, T, d_qk] bf16 saved forward outputs
  *   rstd      in  [2, H, T] float32 saved forward output
@@ -204,7 +210,7 @@ int qkvp_set_wait_timeout_ns(uint64_t ns);
  * is being captured into a CUDA graph), so consecutive events bracket one
  * kernel each.  Order of the kernels: qkvp_quantize_bank: amax, quantise;
  * qkvp_forward: x amax, x quantise, forward GEMM; qkvp_backward: dY amax,
- * dY quantise, dX GEMM, dW GEMM, dW reduction.  n = 0 disarms.  Not
+ * dY quantise, dX GEMM, dW GEMM (with its split reduction).  n = 0 disarms.  Not
  * thread-safe; meant for benchmarks. */
 int qkvp_set_timing_events(void* const* events, int n);
 

@@ -6,3 +6,5 @@ from .qkvp_oracle import (e4m3_decode, e4m3_encode, scale_of, quantize,  # noqa:
                           rope_inverse, rms_norm, packed_gemm, forward,
                           norm_rope_backward, epilogue_backward, grad_gemms,
                           backward, E4M3_MAX)
+from .oproj_oracle import (quantize_weight, oproj_forward, oproj_grad_gemms,  # noqa: F401
+                           oproj_backward)

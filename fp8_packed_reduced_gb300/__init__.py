@@ -75,6 +75,12 @@ def lib() -> ctypes.CDLL:
             "qkvp_set_timing_events": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int]),
             "qkvp_timing_events_recorded": (ctypes.c_int, []),
             "qkvp_set_cta_pairs": (ctypes.c_int, [ctypes.c_int]),
+            "qkvp_weight_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 3),
+            "qkvp_quantize_weight": (ctypes.c_int, [ctypes.c_int] * 3 + [ctypes.POINTER(_P)] + [_P] * 4
+                                     + [ctypes.c_size_t, _P]),
+            "qkvp_oproj_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 3),
+            "qkvp_oproj_forward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 7 + [ctypes.c_size_t, _P]),
+            "qkvp_oproj_backward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 10 + [ctypes.c_size_t, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -352,4 +358,97 @@ def backward(dq, dk, dv, saved: Saved, W8T, w_scale, rope_table, ws=None, out=No
                              _ptr(o["dY8"]), _ptr(o["dy_scale"]), _ptr(ws), ws.numel(),
                              _stream(dev))
     _check(rc, "qkvp_backward")
+    return o
+
+
+# ----------------------------------------------------------------------------
+# Output projection over the V/O bank
+# ----------------------------------------------------------------------------
+
+def quantize_weight(weights: Sequence[torch.Tensor], out=None):
+    """Quantise L bf16 matrices [R, C] (one scale each) into both FP8 layouts.
+
+    Returns (W8 [L, R, C] uint8, W8T [L, C, R] uint8, w_scale [L] float32)."""
+    L = len(weights)
+    R, C = weights[0].shape
+    dev = weights[0].device
+    for l, w in enumerate(weights):
+        _need_cuda(w, f"weight {l}", torch.bfloat16, (R, C))
+    if out is None:
+        W8 = torch.empty((L, R, C), dtype=torch.uint8, device=dev)
+        W8T = torch.empty((L, C, R), dtype=torch.uint8, device=dev)
+        w_scale = torch.empty((L,), dtype=torch.float32, device=dev)
+    else:
+        W8, W8T, w_scale = out
+        _need_cuda(W8, "W8", torch.uint8, (L, R, C))
+        _need_cuda(W8T, "W8T", torch.uint8, (L, C, R))
+        _need_cuda(w_scale, "w_scale", torch.float32, (L,))
+    nws = int(lib().qkvp_weight_workspace_bytes(L, R, C))
+    if nws == 0:
+        raise QKVPError(ERR_UNSUPPORTED, "qkvp_weight_workspace_bytes")
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    arr = (ctypes.c_void_p * L)(*[ctypes.c_void_p(w.data_ptr()) for w in weights])
+    _check(lib().qkvp_quantize_weight(L, R, C, arr, _ptr(W8), _ptr(W8T), _ptr(w_scale), _ptr(ws), nws,
+                                      _stream(dev)), "qkvp_quantize_weight")
+    return W8, W8T, w_scale
+
+
+def new_oproj_workspace(T: int, D: int, K: int, device="cuda") -> torch.Tensor:
+    """A zero-initialised workspace for the O projection's forward/backward."""
+    n = int(lib().qkvp_oproj_workspace_bytes(T, D, K))
+    if n == 0:
+        raise QKVPError(ERR_UNSUPPORTED, "qkvp_oproj_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(lib().qkvp_workspace_init(_ptr(ws), n, _stream(ws.device)), "qkvp_workspace_init")
+    return ws
+
+
+def oproj_forward(a, Wo8, wo_scale, ws=None, out=None):
+    """out [T, D] = FP8 a [T, K] . W_o^T.  Returns (out, a8 [T, K] uint8, a_scale [1])."""
+    T, K = a.shape
+    D = Wo8.shape[0]
+    _need_cuda(a, "a", torch.bfloat16)
+    _need_cuda(Wo8, "Wo8", torch.uint8, (D, K))
+    _need_cuda(wo_scale, "wo_scale", torch.float32, (1,))
+    dev = a.device
+    if ws is None:
+        ws = new_oproj_workspace(T, D, K, dev)
+    if out is None:
+        out = dict(out=torch.empty((T, D), dtype=torch.bfloat16, device=dev),
+                   a8=torch.empty((T, K), dtype=torch.uint8, device=dev),
+                   a_scale=torch.empty((1,), dtype=torch.float32, device=dev))
+    o = out
+    for name, dt, shp in (("out", torch.bfloat16, (T, D)), ("a8", torch.uint8, (T, K)),
+                          ("a_scale", torch.float32, (1,))):
+        _need_cuda(o[name], name, dt, shp)
+    _check(lib().qkvp_oproj_forward(T, D, K, _ptr(a), _ptr(Wo8), _ptr(wo_scale), _ptr(o["out"]), _ptr(o["a8"]),
+                                    _ptr(o["a_scale"]), _ptr(ws), ws.numel(), _stream(dev)), "qkvp_oproj_forward")
+    return o["out"], o["a8"], o["a_scale"]
+
+
+def oproj_backward(dout, Wo8T, wo_scale, a8, a_scale, ws=None, out=None):
+    """Backward of the O projection.  Returns a dict with da [T, K], dWo [D, K]
+    (bf16), dout8 [T, D] (uint8) and dout_scale [1]."""
+    T, D = dout.shape
+    K = Wo8T.shape[0]
+    _need_cuda(dout, "dout", torch.bfloat16)
+    _need_cuda(Wo8T, "Wo8T", torch.uint8, (K, D))
+    _need_cuda(wo_scale, "wo_scale", torch.float32, (1,))
+    _need_cuda(a8, "a8", torch.uint8, (T, K))
+    _need_cuda(a_scale, "a_scale", torch.float32, (1,))
+    dev = dout.device
+    if ws is None:
+        ws = new_oproj_workspace(T, D, K, dev)
+    if out is None:
+        out = dict(da=torch.empty((T, K), dtype=torch.bfloat16, device=dev),
+                   dWo=torch.empty((D, K), dtype=torch.bfloat16, device=dev),
+                   dout8=torch.empty((T, D), dtype=torch.uint8, device=dev),
+                   dout_scale=torch.empty((1,), dtype=torch.float32, device=dev))
+    o = out
+    for name, dt, shp in (("da", torch.bfloat16, (T, K)), ("dWo", torch.bfloat16, (D, K)),
+                          ("dout8", torch.uint8, (T, D)), ("dout_scale", torch.float32, (1,))):
+        _need_cuda(o[name], name, dt, shp)
+    _check(lib().qkvp_oproj_backward(T, D, K, _ptr(dout), _ptr(Wo8T), _ptr(wo_scale), _ptr(a8), _ptr(a_scale),
+                                     _ptr(o["da"]), _ptr(o["dWo"]), _ptr(o["dout8"]), _ptr(o["dout_scale"]),
+                                     _ptr(ws), ws.numel(), _stream(dev)), "qkvp_oproj_backward")
     return o

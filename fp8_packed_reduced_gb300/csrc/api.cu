@@ -98,15 +98,16 @@ constexpr int kMaxSplits = 16;
 struct DwShape {
   int bn, m_tiles, n_tiles, kblocks_total;
 };
-DwShape dw_shape(const qkvp_dims* d) {
-  const int N = d->H * (2 * d->d_qk + d->d_v);
+// Tiles of a split-over-tokens weight gradient [R, C] from T tokens.
+DwShape dw_shape_rc(int R, int C, int T) {
   DwShape s;
-  s.bn = d->D % 256 == 0 ? 256 : 128;
-  s.m_tiles = (N + 127) / 128;
-  s.n_tiles = d->D / s.bn;
-  s.kblocks_total = (d->T + 127) / 128;
+  s.bn = C % 256 == 0 ? 256 : 128;
+  s.m_tiles = (R + 127) / 128;
+  s.n_tiles = C / s.bn;
+  s.kblocks_total = (T + 127) / 128;
   return s;
 }
+DwShape dw_shape(const qkvp_dims* d) { return dw_shape_rc(d->H * (2 * d->d_qk + d->d_v), d->D, d->T); }
 size_t dw_partial_bytes(const DwShape& s, int splits) {
   return static_cast<size_t>(splits) * s.m_tiles * s.n_tiles * s.bn * 128 * sizeof(float);
 }
@@ -114,10 +115,10 @@ size_t dw_partial_bytes(const DwShape& s, int splits) {
 size_t dw_counter_bytes(const DwShape& s) {
   return (static_cast<size_t>(s.m_tiles) * s.n_tiles * kDwEpiWarps * sizeof(int) + 255) / 256 * 256;
 }
-size_t ws_bytes_for(const qkvp_dims* d) {
-  const DwShape s = dw_shape(d);
+size_t ws_bytes_for_shape(const DwShape& s) {
   return kStatusBytes + 2 * kPartsBytes + dw_counter_bytes(s) + dw_partial_bytes(s, kMaxSplits);
 }
+size_t ws_bytes_for(const qkvp_dims* d) { return ws_bytes_for_shape(dw_shape(d)); }
 
 // Split count for the dW GEMM: the fewest splits whose units fill the
 // workers (SMs, or SM pairs) in whole waves to >= 90%, with at least 4
@@ -164,6 +165,78 @@ void mark(cudaStream_t s) {
   do {                                               \
     if ((expr) != cudaSuccess) return QKVP_ERR_CUDA; \
   } while (0)
+
+// Per-tensor quantisation of a bf16 activation of n elements (n % 16 == 0):
+// amax partials, then codes and the scale (two launches).
+int quantize_activation(const uint16_t* x, int64_t n, uint8_t* x8, float* parts, float* scale, int sms,
+                        cudaStream_t s) {
+  const int nparts = std::min(kMaxParts, 4 * sms);
+  mark(s);
+  QKVP_TRY_CUDA(launch_amax_bf16(x, n, parts, nparts, s));
+  mark(s);
+  QKVP_TRY_CUDA(launch_x_quant(x, n, x8, parts, nparts, scale, 4 * sms, s));
+  mark(s);
+  return QKVP_OK;
+}
+
+// out [T, Nout] bf16 = (A8 [T, K] . B8 [Nout, K]^T) * sa * sb, both operands
+// K-major codes (the dX GEMM body).  K and Nout multiples of 128.
+int gemm_nt(int T, int Nout, int K, const uint8_t* A8, const uint8_t* B8, const float* sa, const float* sb,
+            uint16_t* out, DevStatus st, int sms, cudaStream_t s) {
+  const int bn = Nout % 256 == 0 ? 256 : 128;   // one box per stage: the whole B tile (this CTA's half on pairs)
+  const int pair = (g_pair_mask & 2) ? 2 : 1;
+  CUtensorMap tm_a, tm_b, tm_out;
+  bool ok = map2d(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A8, K, T, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B8, K, Nout, K, 128, bn / pair, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, Nout, T, Nout * 2ull, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!ok) return QKVP_ERR_CUDA;
+  DxParams gp;
+  gp.T = T;
+  gp.D = Nout;
+  gp.bn = bn;
+  gp.n_tiles = Nout / bn;
+  gp.pair = pair;
+  gp.num_units = ((T + 127) / 128 + pair - 1) / pair * gp.n_tiles;
+  gp.kblocks = (K + 127) / 128;
+  gp.dy_scale = sa;
+  gp.w_scale = sb;
+  QKVP_TRY_CUDA(launch_dx_gemm(tm_a, tm_b, tm_out, gp, sms, st, s));
+  mark(s);
+  return QKVP_OK;
+}
+
+// dW [R, C] bf16 = (G8 [T, R]^T . X8 [T, C]) * sg * sx, both operands read
+// MN-major (token-major codes as stored), split over the tokens; partials and
+// per-tile counters in the workspace (`ds` describes their layout).
+int gemm_tn_split(int T, int R, int C, const DwShape& ds, const uint8_t* G8, const uint8_t* X8, const float* sg,
+                  const float* sx, uint16_t* dW, int* counters, float* partials, DevStatus st, int sms,
+                  cudaStream_t s) {
+  CUtensorMap tm_g, tm_x;
+  bool ok = map2d(&tm_g, CU_TENSOR_MAP_DATA_TYPE_UINT8, G8, R, T, R, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, X8, C, T, C, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return QKVP_ERR_CUDA;
+  DwParams wp;
+  wp.N = R;
+  wp.D = C;
+  wp.bn = ds.bn;
+  wp.m_tiles = ds.m_tiles;
+  wp.n_tiles = ds.n_tiles;
+  wp.kblocks_total = ds.kblocks_total;
+  // pairs split the 256 columns of a tile: one 128-column box of X8 each
+  wp.pair = ((g_pair_mask & 4) && ds.bn == 256) ? 2 : 1;
+  const int pair_tiles = (ds.m_tiles + wp.pair - 1) / wp.pair * ds.n_tiles;
+  wp.splits = choose_splits(pair_tiles, ds.kblocks_total, sms / wp.pair);
+  wp.num_units = wp.splits * pair_tiles;
+  wp.partials = partials;
+  wp.counters = counters;
+  wp.dy_scale = sg;
+  wp.x_scale = sx;
+  wp.dW = dW;
+  QKVP_TRY_CUDA(launch_dw_gemm(tm_g, tm_x, wp, sms, st, s));
+  mark(s);
+  return QKVP_OK;
+}
 
 }  // namespace
 
@@ -326,13 +399,8 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return QKVP_ERR_CUDA;
 
-  const int nparts = std::min(kMaxParts, 4 * sms);
-  const int64_t n = static_cast<int64_t>(T) * D;
-  mark(s);
-  QKVP_TRY_CUDA(launch_amax_bf16(x, n, xparts, nparts, s));
-  mark(s);
-  QKVP_TRY_CUDA(launch_x_quant(x, n, x8, xparts, nparts, x_scale, 4 * sms, s));
-  mark(s);
+  rc = quantize_activation(x, static_cast<int64_t>(T) * D, x8, xparts, x_scale, sms, s);
+  if (rc != QKVP_OK) return rc;
 
   FwdParams p;
   p.T = T;
@@ -394,15 +462,6 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   ok = ok && map3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&m.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, dvw, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map2d(&m.dy8, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_32B);
-  // dY8 [T, N] read as 128 x 128 tiles: K-major A of the dX GEMM, MN-major A of the dW GEMM
-  CUtensorMap tm_dy, tm_w8t, tm_dx, tm_x8;
-  ok = ok && map2d(&tm_dy, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  const int dx_bn = D % 256 == 0 ? 256 : 128;   // one box per stage: the whole B tile (this CTA's half on pairs)
-  const int dx_pair = (g_pair_mask & 2) ? 2 : 1;
-  ok = ok && map2d(&tm_w8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8T, N, D, N, 128, dx_bn / dx_pair,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dx, D, T, D * 2ull, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map2d(&tm_x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, D, T, D, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return QKVP_ERR_CUDA;
 
   BwdParams bp;
@@ -426,40 +485,114 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   QKVP_TRY_CUDA(launch_bwd_quant(m, bp, std::min(bp.num_units, sms), st, s));
   mark(s);
 
-  DxParams xp;
-  xp.T = T;
-  xp.D = D;
-  xp.bn = dx_bn;
-  xp.n_tiles = D / xp.bn;
-  xp.pair = dx_pair;
-  xp.num_units = (tiles + dx_pair - 1) / dx_pair * xp.n_tiles;
-  xp.kblocks = (N + 127) / 128;
-  xp.dy_scale = dy_scale;
-  xp.w_scale = w_scale;
-  QKVP_TRY_CUDA(launch_dx_gemm(tm_dy, tm_w8t, tm_dx, xp, sms, st, s));
-  mark(s);
+  // dX [T, D] = dY8 [T, N] . W8 with the cached W8T [D, N] as the K-major operand
+  rc = gemm_nt(T, D, N, dY8, W8T, dy_scale, w_scale, dx, st, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // dW [N, D] = dY8^T . x8, both read MN-major
+  rc = gemm_tn_split(T, N, D, dw_shape(dims), dY8, x8, dy_scale, x_scale, dW, dwcount, dwparts, st, sms, s);
+  if (rc != QKVP_OK) return rc;
+  return QKVP_OK;
+}
 
-  const DwShape ds = dw_shape(dims);
-  DwParams wp;
-  wp.N = N;
-  wp.D = D;
-  wp.bn = ds.bn;
-  wp.m_tiles = ds.m_tiles;
-  wp.n_tiles = ds.n_tiles;
-  wp.kblocks_total = ds.kblocks_total;
-  // pairs split the 256 columns of a tile: one 128-column box of x8 each
-  wp.pair = ((g_pair_mask & 4) && ds.bn == 256) ? 2 : 1;
-  const int pair_tiles = (ds.m_tiles + wp.pair - 1) / wp.pair * ds.n_tiles;
-  wp.splits = choose_splits(pair_tiles, ds.kblocks_total, sms / wp.pair);
-  wp.num_units = wp.splits * pair_tiles;
-  wp.partials = dwparts;
-  wp.counters = dwcount;
-  wp.dy_scale = dy_scale;
-  wp.x_scale = x_scale;
-  wp.dW = dW;
-  QKVP_TRY_CUDA(launch_dw_gemm(tm_dy, tm_x8, wp, sms, st, s));
+// ---------------------------------------------------------------------------
+// Weight refresh for single matrices and the O projection over the V/O bank
+// ---------------------------------------------------------------------------
+size_t qkvp_weight_workspace_bytes(int L, int R, int C) {
+  if (L < 1 || L > kMaxLayers || R < 128 || C < 128 || R % 128 || C % 128 || R > 65536 || C > 16384) return 0;
+  return kStatusBytes + static_cast<size_t>(L) * kBankAmaxBlocks * sizeof(float);
+}
+
+int qkvp_quantize_weight(int L, int R, int C, const uint16_t* const* W, uint8_t* W8, uint8_t* W8T, float* w_scale,
+                         void* ws, size_t ws_bytes, void* stream) {
+  if (L < 1 || !W || !W8 || !W8T || !w_scale || !ws || R < 1 || C < 1) return QKVP_ERR_INVALID_ARGUMENT;
+  const size_t need = qkvp_weight_workspace_bytes(L, R, C);
+  if (need == 0) return QKVP_ERR_UNSUPPORTED;
+  // the bank kernels with empty Q and K packs: every row comes from W[l]
+  BankArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int l = 0; l < L; ++l) {
+    if (!W[l]) return QKVP_ERR_INVALID_ARGUMENT;
+    if (!aligned16(W[l])) return QKVP_ERR_MISALIGNED;
+    a.Wq[l] = a.Wk[l] = a.Wv[l] = W[l];
+  }
+  if (!aligned16(W8) || !aligned16(W8T) || !aligned16(w_scale) || !aligned16(ws)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < need) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  a.W8 = W8;
+  a.W8T = W8T;
+  a.w_scale = w_scale;
+  a.L = L;
+  a.D = C;
+  a.Nq = 0;
+  a.N = R;
+  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  mark(s);
+  QKVP_TRY_CUDA(launch_bank_amax(a, partials, s));
+  mark(s);
+  QKVP_TRY_CUDA(launch_bank_quant(a, partials, s));
   mark(s);
   return QKVP_OK;
+}
+
+namespace {
+int check_oproj(int T, int D, int K) {
+  if (T < 1 || D < 1 || K < 1) return QKVP_ERR_INVALID_ARGUMENT;
+  if (T > (1 << 24) || D % 128 || K % 128 || D > 16384 || K > 16384) return QKVP_ERR_UNSUPPORTED;
+  return QKVP_OK;
+}
+}  // namespace
+
+size_t qkvp_oproj_workspace_bytes(int T, int D, int K) {
+  if (check_oproj(T, D, K) != QKVP_OK) return 0;
+  return ws_bytes_for_shape(dw_shape_rc(D, K, T));
+}
+
+int qkvp_oproj_forward(int T, int D, int K, const uint16_t* a, const uint8_t* Wo8, const float* wo_scale,
+                       uint16_t* out, uint8_t* a8, float* a_scale, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_oproj(T, D, K);
+  if (rc != QKVP_OK) return rc;
+  if (!a || !Wo8 || !wo_scale || !out || !a8 || !a_scale || !ws) return QKVP_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {a, Wo8, wo_scale, out, a8, a_scale, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < qkvp_oproj_workspace_bytes(T, D, K)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return QKVP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* aparts = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  rc = quantize_activation(a, static_cast<int64_t>(T) * K, a8, aparts, a_scale, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // out [T, D] = a8 [T, K] . Wo8 [D, K]^T
+  return gemm_nt(T, D, K, a8, Wo8, a_scale, wo_scale, out, dev_status(ws), sms, s);
+}
+
+int qkvp_oproj_backward(int T, int D, int K, const uint16_t* dout, const uint8_t* Wo8T, const float* wo_scale,
+                        const uint8_t* a8, const float* a_scale, uint16_t* da, uint16_t* dWo, uint8_t* dout8,
+                        float* dout_scale, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_oproj(T, D, K);
+  if (rc != QKVP_OK) return rc;
+  if (!dout || !Wo8T || !wo_scale || !a8 || !a_scale || !da || !dWo || !dout8 || !dout_scale || !ws)
+    return QKVP_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {dout, Wo8T, wo_scale, a8, a_scale, da, dWo, dout8, dout_scale, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < qkvp_oproj_workspace_bytes(T, D, K)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return QKVP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* gparts = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
+  const DwShape ds = dw_shape_rc(D, K, T);
+  int* dwcount = reinterpret_cast<int*>(wsb + kStatusBytes + 2 * kPartsBytes);
+  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes + dw_counter_bytes(ds));
+  const DevStatus st = dev_status(ws);
+  rc = quantize_activation(dout, static_cast<int64_t>(T) * D, dout8, gparts, dout_scale, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // da [T, K] = dout8 [T, D] . Wo8 with the cached Wo8T [K, D] as the K-major operand
+  rc = gemm_nt(T, K, D, dout8, Wo8T, dout_scale, wo_scale, da, st, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // dWo [D, K] = dout8^T . a8, both read MN-major
+  return gemm_tn_split(T, D, K, ds, dout8, a8, dout_scale, a_scale, dWo, dwcount, dwparts, st, sms, s);
 }
 
 }  // extern "C"

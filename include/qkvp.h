@@ -228,6 +228,60 @@ int qkvp_timing_events_recorded(void);
  * thread-safe; meant for tests and tuning.  Default 6 (dX and dW paired). */
 int qkvp_set_cta_pairs(int mask);
 
+/* ------------------------------------------------------------------------
+ * Output projection over the V/O bank ("Track 1 ... packed FP8 attention",
+ * section "Changes": Q/K are stored apart from the rectangular V/O bank; FP8
+ * weight layouts cached once per optimizer update from one read).  The step
+ * after attention: out = a . W_o^T, with a [T, K] the heads' outputs side by
+ * side (K = H * d_v) and W_o [D, K] (out x in).  Same FP8 recipe as the
+ * packed projection: per-tensor E4M3 scales amax/448 for a, W_o and dout.
+ * Shapes: T 1 .. 2^24; D and K multiples of 128, at most 16384.
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of scratch qkvp_quantize_weight needs for L matrices [R, C] (0 if
+ * unsupported: R, C multiples of 128, R <= 65536, C <= 16384, L <= 128). */
+size_t qkvp_weight_workspace_bytes(int L, int R, int C);
+
+/* Refresh of L weight matrices, once per optimizer update: one scale per
+ * matrix and its codes in both layouts from one read of the weight.
+ *   W      HOST array of L device pointers to bf16 [R, C] (row-major)
+ *   W8     out, device, [L, R, C] codes      W8T out, device, [L, C, R] codes
+ *   w_scale out, device, [L] float32
+ *   ws     device scratch of qkvp_weight_workspace_bytes(L, R, C) bytes      */
+int qkvp_quantize_weight(int L, int R, int C, const uint16_t* const* W,
+                         uint8_t* W8, uint8_t* W8T, float* w_scale,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes of scratch qkvp_oproj_forward / qkvp_oproj_backward need (one
+ * workspace serves both; zero it once with qkvp_workspace_init, and again
+ * after a device error).  0 if the shape is unsupported. */
+size_t qkvp_oproj_workspace_bytes(int T, int D, int K);
+
+/* Forward: a is quantised with its own scale, then
+ *   out = (a8 . Wo8^T) * s_a * s_o     (one FP8 GEMM, fp32 accumulate)
+ *   a        in  [T, K] bf16           Wo8 in [D, K] codes, wo_scale [1]
+ *   out      out [T, D] bf16
+ *   a8       out [T, K] codes (saved for the backward), a_scale out [1]  */
+int qkvp_oproj_forward(int T, int D, int K, const uint16_t* a,
+                       const uint8_t* Wo8, const float* wo_scale,
+                       uint16_t* out, uint8_t* a8, float* a_scale,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Backward: dout is quantised with its own scale into dout8, then
+ *   da  = (dout8 . Wo8) * s_g * s_o    with the cached Wo8T as the K-major operand
+ *   dWo = (dout8^T . a8) * s_g * s_a   split over tokens, reduced in split
+ *                                      order inside the GEMM (deterministic)
+ *   dout     in  [T, D] bf16           Wo8T in [K, D] codes, wo_scale [1]
+ *   a8       in  [T, K] codes from the forward, a_scale [1]
+ *   da       out [T, K] bf16           dWo out [D, K] bf16 (overwritten)
+ *   dout8    out [T, D] codes          dout_scale out [1] float32           */
+int qkvp_oproj_backward(int T, int D, int K, const uint16_t* dout,
+                        const uint8_t* Wo8T, const float* wo_scale,
+                        const uint8_t* a8, const float* a_scale,
+                        uint16_t* da, uint16_t* dWo,
+                        uint8_t* dout8, float* dout_scale,
+                        void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -97,6 +97,15 @@ def bank_layers(L: int, H: int, D: int, d_qk: int = 96, d_v: int = 128, seed: in
     return out
 
 
+def oproj_inputs(T: int, D: int, K: int, seed: int = 0, device="cpu"):
+    """Output projection: the heads' attention outputs a [T, K] ~ N(0, 1),
+    W_o [D, K] ~ N(0, 1/K) (fan-in K) and the upstream gradient dout [T, D]
+    ~ N(0, 1), all bf16; generators seeded seed+20, +21, +22."""
+    return dict(a=_normal((T, K), 1.0, seed + 20, device),
+                Wo=_normal((D, K), K ** -0.5, seed + 21, device),
+                dout=_normal((T, D), 1.0, seed + 22, device))
+
+
 def to_numpy_f32(t: torch.Tensor):
     """bf16/float tensor -> float32 NumPy array holding the same values."""
     return t.detach().to("cpu", torch.float32).numpy()

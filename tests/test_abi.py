@@ -125,6 +125,32 @@ def test_other_validation_codes(qk):
     assert lib.qkvp_set_cta_pairs(prev) == 3
 
 
+def test_oproj_validation_codes(qk):
+    lib = qk.lib()
+    p = ctypes.c_void_p(4096)
+    assert lib.qkvp_oproj_workspace_bytes(128, 768, 768) > 0
+    assert lib.qkvp_oproj_workspace_bytes(128, 700, 768) == 0
+    assert lib.qkvp_weight_workspace_bytes(1, 768, 768) > 0
+    assert lib.qkvp_weight_workspace_bytes(1, 100, 768) == 0
+    fwd = lib.qkvp_oproj_forward
+    assert fwd(0, 768, 768, p, p, p, p, p, p, p, 1 << 40, None) == qk.ERR_INVALID_ARGUMENT
+    assert fwd(128, 700, 768, p, p, p, p, p, p, p, 1 << 40, None) == qk.ERR_UNSUPPORTED
+    assert fwd(128, 768, 768, None, p, p, p, p, p, p, 1 << 40, None) == qk.ERR_INVALID_ARGUMENT
+    assert fwd(128, 768, 768, ctypes.c_void_p(4100), p, p, p, p, p, p, 1 << 40, None) == qk.ERR_MISALIGNED
+    assert fwd(128, 768, 768, p, p, p, p, p, p, p, 64, None) == qk.ERR_WORKSPACE_TOO_SMALL
+    bwd = lib.qkvp_oproj_backward
+    assert bwd(128, 768, 768, p, p, p, p, p, p, p, p, None, p, 1 << 40, None) == qk.ERR_INVALID_ARGUMENT
+    assert bwd(128, 768, 640 + 1, p, p, p, p, p, p, p, p, p, p, 1 << 40, None) == qk.ERR_UNSUPPORTED
+    assert bwd(128, 768, 768, p, p, p, p, p, p, p, p, p, p, 64, None) == qk.ERR_WORKSPACE_TOO_SMALL
+    arr = (ctypes.c_void_p * 1)(ctypes.c_void_p(4096))
+    qw = lib.qkvp_quantize_weight
+    assert qw(0, 768, 768, arr, p, p, p, p, 1 << 20, None) == qk.ERR_INVALID_ARGUMENT
+    assert qw(1, 768, 700, arr, p, p, p, p, 1 << 20, None) == qk.ERR_UNSUPPORTED
+    assert qw(1, 768, 768, (ctypes.c_void_p * 1)(ctypes.c_void_p(4098)), p, p, p, p, 1 << 20, None) \
+        == qk.ERR_MISALIGNED
+    assert qw(1, 768, 768, arr, p, p, p, p, 8, None) == qk.ERR_WORKSPACE_TOO_SMALL
+
+
 def test_product_path_refuses_without_library(tmp_path, monkeypatch):
     import fp8_packed_reduced_gb300 as pkg
     monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "missing.so"))

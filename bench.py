@@ -61,31 +61,36 @@ def algorithmic_work(s: synth.Shape):
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from the
 # ncu captures summarised in profiles/ncu_*_T24576_D768.md, taken at T = 24576
-# and scaled to the workload by its tokens.  They describe the kernel sources
-# whose digest is recorded here and are reported as null for any other build.
+# and scaled to the workload by its tokens.  Each figure describes the device
+# code of its kernel as it was captured (the digest of the kernel's source
+# file and the shared device headers) and is reported as null for any other.
+KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu"}
 TRAFFIC = {
-    "sources_sha256": "aacba0465e69c6eb24a720b7dde9e918172064b86189fe10decb1540fc443ed9",
     "T": 24576,
-    "bytes": {"dy_amax": 159.37e6, "dy_quant": 181.00e6, "fwd_gemm": 64.65e6, "dx_gemm": 52.55e6,
-              "dw_gemm": 69.47e6},
+    "sources_sha256": {"bwd": "5cddaa41ab74c2ce6464ba9ac423bbc2b9e9d1d0ac201d9dfe2a9356cfedc022", "gemm": "4402b4c9e7e3d5472575b4a8b29698e6023b08771c5b49bc6fa180182fab8d00"},
+    "bytes": {"dy_amax": ("bwd", 159.37e6), "dy_quant": ("bwd", 181.00e6), "fwd_gemm": ("gemm", 64.65e6),
+              "dx_gemm": ("gemm", 52.55e6), "dw_gemm": ("gemm", 69.47e6)},
 }
 
 
-def sources_sha256() -> str:
-    """Digest of the CUDA sources and the C ABI header of the library."""
+def sources_sha256(unit: str) -> str:
+    """Digest of one kernel source file with the device headers it includes."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_packed_reduced_gb300", "csrc")
-    paths = [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith((".cu", ".cuh"))]
-    for path in paths + [os.path.join(ROOT, "include", "qkvp.h")]:
+    for path in (os.path.join(csrc, KERNEL_SOURCES[unit]), os.path.join(csrc, "common.cuh"),
+                 os.path.join(csrc, "kernels.cuh")):
         h.update(os.path.basename(path).encode())
         h.update(open(path, "rb").read())
     return h.hexdigest()
 
 
 def traffic_for(kernel: str, T: int):
-    b = TRAFFIC["bytes"].get(kernel)
-    if b is None or sources_sha256() != TRAFFIC["sources_sha256"]:
+    entry = TRAFFIC["bytes"].get(kernel)
+    if entry is None:
+        return None
+    unit, b = entry
+    if sources_sha256(unit) != TRAFFIC["sources_sha256"][unit]:
         return None
     return round(b * T / TRAFFIC["T"])
 
@@ -206,6 +211,24 @@ class Step:
         qk.backward(self.dq, self.dk, self.dv, saved, W8T[0], ws_[0:1], self.table, ws=self.ws, out=self.bwd_out)
 
 
+def kernel_table(per, work, peaks):
+    """Per-kernel mean time, achieved algorithmic rate and fraction of the
+    measured peak (HBM copy GB/s, or sustained bf16 x 2 for E4M3 GEMMs)."""
+    fp8_sus = 2.0 * peaks["bf16_sus"]       # E4M3 dense = 2 x bf16 dense (nominal ratio)
+    kern = {}
+    for name, (bound, amount) in work.items():
+        t = per[name] * 1e-3
+        if bound == "hbm":
+            ach = amount / t / 1e9
+            kern[name] = dict(ms=round(per[name], 5), bound="hbm", achieved=round(ach, 1), unit="GB/s",
+                              frac=round(ach / peaks["hbm"], 4))
+        else:
+            ach = amount / t / 1e12
+            kern[name] = dict(ms=round(per[name], 5), bound="tensor", achieved=round(ach, 1), unit="TFLOP/s",
+                              frac=round(ach / fp8_sus, 4))
+    return kern
+
+
 def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -281,18 +304,7 @@ def run_ours(args, rank, world):
     work = algorithmic_work(s)
     peaks = load_peaks()
     fp8_sus = 2.0 * peaks["bf16_sus"]       # E4M3 dense = 2 x bf16 dense (nominal ratio)
-    kern = {}
-    for name in KERNELS:
-        bound, amount = work[name]
-        t = per[name] * 1e-3
-        if bound == "hbm":
-            ach = amount / t / 1e9
-            kern[name] = dict(ms=round(per[name], 5), bound="hbm", achieved=round(ach, 1), unit="GB/s",
-                              frac=round(ach / peaks["hbm"], 4))
-        else:
-            ach = amount / t / 1e12
-            kern[name] = dict(ms=round(per[name], 5), bound="tensor", achieved=round(ach, 1), unit="TFLOP/s",
-                              frac=round(ach / fp8_sus, 4))
+    kern = kernel_table(per, work, peaks)
     dom = max(KERNELS, key=lambda k: per[k])
     bound, amount = work[dom]
     roofline = dict(kernel=dom, bound=bound, achieved=kern[dom]["achieved"],
@@ -318,9 +330,79 @@ def run_ours(args, rank, world):
         "launch": "the K timed steps replayed as one captured CUDA graph",
         "clocks": clocks, "e2e": e2e,
     }
+    if not args.no_oproj:
+        line["next_rows"] = {"oproj": run_oproj(args, dev, world)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, args.cpu_sample)
     return line
+
+
+OPROJ_KERNELS = ["w_amax", "w_quant", "a_amax", "a_quant", "out_gemm", "g_amax", "g_quant", "da_gemm", "dwo_gemm"]
+OPROJ_SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (5, 6), (7, 8), (8, 9), (9, 10), (10, 11)]
+OPROJ_EVENTS = 12
+
+
+def run_oproj(args, dev, world):
+    """The output projection over the V/O bank (weight refresh + forward +
+    backward) on the same token count, D = K = H * d_v, timed like the main
+    step: K steps captured in one CUDA graph, per-kernel events inside it."""
+    import fp8_packed_reduced_gb300 as qk
+    T, D, K = args.T, args.D, args.H * 128
+    inp = synth.oproj_inputs(T, D, K, seed=0, device=dev)
+    u8, bf, f = (dict(dtype=torch.uint8, device=dev), dict(dtype=torch.bfloat16, device=dev),
+                 dict(dtype=torch.float32, device=dev))
+    wbuf = (torch.empty((1, D, K), **u8), torch.empty((1, K, D), **u8), torch.empty((1,), **f))
+    fo = dict(out=torch.empty((T, D), **bf), a8=torch.empty((T, K), **u8), a_scale=torch.empty((1,), **f))
+    bo = dict(da=torch.empty((T, K), **bf), dWo=torch.empty((D, K), **bf), dout8=torch.empty((T, D), **u8),
+              dout_scale=torch.empty((1,), **f))
+    ws = qk.new_oproj_workspace(T, D, K, dev)
+
+    def step():
+        W8, W8T, so = qk.quantize_weight([inp["Wo"]], out=wbuf)
+        _, a8, sa = qk.oproj_forward(inp["a"], W8[0], so[0:1], ws=ws, out=fo)
+        qk.oproj_backward(inp["dout"], W8T[0], so[0:1], a8, sa, ws=ws, out=bo)
+
+    steps = max(3, min(args.steps, 100))
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(OPROJ_EVENTS)] for _ in range(steps)]
+    stream = torch.cuda.current_stream(dev)
+    for ev in events:
+        for e in ev:
+            e.record(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(steps):
+            qk.set_timing_events(events[i])
+            step()
+        qk.set_timing_events([])
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1) / steps, world, dev)
+    code, where = qk.poll_device_status(ws)
+    if code != 0:
+        raise RuntimeError(f"device status {qk.STATUS.get(code)} from kernel {where}")
+    per = {k: 0.0 for k in OPROJ_KERNELS}
+    for ev in events:
+        for name, (a, b_) in zip(OPROJ_KERNELS, OPROJ_SPANS):
+            per[name] += ev[a].elapsed_time(ev[b_]) / steps
+    flops = 2.0 * T * D * K
+    work = {"w_amax": ("hbm", D * K * 2), "w_quant": ("hbm", D * K * 4), "a_amax": ("hbm", T * K * 2),
+            "a_quant": ("hbm", T * K * 3), "out_gemm": ("tensor", flops), "g_amax": ("hbm", T * D * 2),
+            "g_quant": ("hbm", T * D * 3), "da_gemm": ("tensor", flops), "dwo_gemm": ("tensor", flops)}
+    kern = kernel_table(per, work, load_peaks())
+    return {"workload": f"output projection over the V/O bank fwd+bwd, T={T}, D={D}, K=H*d_v={K}, "
+                        "weight refresh per step",
+            "value": round(job_tokens_per_s(T, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+            "steps": steps, "kernels": kern, "gpu_launches": len(OPROJ_KERNELS) * steps}
 
 
 def run_e2e(st: Step, args, dev, world):
@@ -431,6 +513,7 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=8192, help="tokens the oracle times for cpu_baseline")
     ap.add_argument("--ref-sample", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-oproj", action="store_true", help="skip the output-projection measurement")
     ap.add_argument("--cta-pairs", type=int, default=None,
                     help="GEMMs on 2-CTA clusters: bit 0 forward, bit 1 dX, bit 2 dW (default: the library's)")
     args = ap.parse_args()

@@ -8,3 +8,5 @@ from .qkvp_oracle import (e4m3_decode, e4m3_encode, scale_of, quantize,  # noqa:
                           backward, E4M3_MAX)
 from .oproj_oracle import (quantize_weight, oproj_forward, oproj_grad_gemms,  # noqa: F401
                            oproj_backward)
+from .mlp_oracle import (to_bf16, mlp_forward, mlp_dpre, mlp_grad_gemms,  # noqa: F401
+                         mlp_backward)

@@ -81,6 +81,9 @@ def lib() -> ctypes.CDLL:
             "qkvp_oproj_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 3),
             "qkvp_oproj_forward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 7 + [ctypes.c_size_t, _P]),
             "qkvp_oproj_backward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 10 + [ctypes.c_size_t, _P]),
+            "qkvp_mlp_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 3),
+            "qkvp_mlp_forward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 12 + [ctypes.c_size_t, _P]),
+            "qkvp_mlp_backward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 18 + [ctypes.c_size_t, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -451,4 +454,87 @@ def oproj_backward(dout, Wo8T, wo_scale, a8, a_scale, ws=None, out=None):
     _check(lib().qkvp_oproj_backward(T, D, K, _ptr(dout), _ptr(Wo8T), _ptr(wo_scale), _ptr(a8), _ptr(a_scale),
                                      _ptr(o["da"]), _ptr(o["dWo"]), _ptr(o["dout8"]), _ptr(o["dout_scale"]),
                                      _ptr(ws), ws.numel(), _stream(dev)), "qkvp_oproj_backward")
+    return o
+
+
+# ----------------------------------------------------------------------------
+# FP8 ReLU-squared MLP
+# ----------------------------------------------------------------------------
+
+def new_mlp_workspace(T: int, D: int, F: int, device="cuda") -> torch.Tensor:
+    """A zero-initialised workspace for the MLP's forward/backward."""
+    n = int(lib().qkvp_mlp_workspace_bytes(T, D, F))
+    if n == 0:
+        raise QKVPError(ERR_UNSUPPORTED, "qkvp_mlp_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(lib().qkvp_workspace_init(_ptr(ws), n, _stream(ws.device)), "qkvp_workspace_init")
+    return ws
+
+
+def mlp_forward(x, W1_8, w1_scale, W2_8, w2_scale, ws=None, out=None):
+    """out = relu(x . W_fc^T)^2 . W_proj^T in FP8.  Returns a dict with out
+    [T, D] bf16, x8 [T, D], x_scale, h [T, F] bf16, h8 [T, F], h_scale."""
+    T, D = x.shape
+    F_ = W1_8.shape[0]
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(W1_8, "W1_8", torch.uint8, (F_, D))
+    _need_cuda(W2_8, "W2_8", torch.uint8, (D, F_))
+    _need_cuda(w1_scale, "w1_scale", torch.float32, (1,))
+    _need_cuda(w2_scale, "w2_scale", torch.float32, (1,))
+    dev = x.device
+    if ws is None:
+        ws = new_mlp_workspace(T, D, F_, dev)
+    if out is None:
+        u8, bf, f = (dict(dtype=torch.uint8, device=dev), dict(dtype=torch.bfloat16, device=dev),
+                     dict(dtype=torch.float32, device=dev))
+        out = dict(out=torch.empty((T, D), **bf), x8=torch.empty((T, D), **u8), x_scale=torch.empty((1,), **f),
+                   h=torch.empty((T, F_), **bf), h8=torch.empty((T, F_), **u8), h_scale=torch.empty((1,), **f))
+    o = out
+    for name, dt, shp in (("out", torch.bfloat16, (T, D)), ("x8", torch.uint8, (T, D)),
+                          ("x_scale", torch.float32, (1,)), ("h", torch.bfloat16, (T, F_)),
+                          ("h8", torch.uint8, (T, F_)), ("h_scale", torch.float32, (1,))):
+        _need_cuda(o[name], name, dt, shp)
+    _check(lib().qkvp_mlp_forward(T, D, F_, _ptr(x), _ptr(W1_8), _ptr(w1_scale), _ptr(W2_8), _ptr(w2_scale),
+                                  _ptr(o["out"]), _ptr(o["x8"]), _ptr(o["x_scale"]), _ptr(o["h"]), _ptr(o["h8"]),
+                                  _ptr(o["h_scale"]), _ptr(ws), ws.numel(), _stream(dev)), "qkvp_mlp_forward")
+    return o
+
+
+def mlp_backward(dout, W1_8T, w1_scale, W2_8T, w2_scale, saved, ws=None, out=None):
+    """Backward of mlp_forward from its saved codes (``saved``: the forward's
+    dict, whose x8, x_scale, h8 and h_scale are read).  Returns a dict with dx
+    [T, D], dW1 [F, D], dW2 [D, F] (bf16), dout8, dout_scale, dpre [T, F] bf16,
+    dpre8 and dpre_scale."""
+    T, D = dout.shape
+    F_ = W2_8T.shape[0]
+    _need_cuda(dout, "dout", torch.bfloat16)
+    _need_cuda(W1_8T, "W1_8T", torch.uint8, (D, F_))
+    _need_cuda(W2_8T, "W2_8T", torch.uint8, (F_, D))
+    _need_cuda(w1_scale, "w1_scale", torch.float32, (1,))
+    _need_cuda(w2_scale, "w2_scale", torch.float32, (1,))
+    _need_cuda(saved["x8"], "saved x8", torch.uint8, (T, D))
+    _need_cuda(saved["x_scale"], "saved x_scale", torch.float32, (1,))
+    _need_cuda(saved["h8"], "saved h8", torch.uint8, (T, F_))
+    _need_cuda(saved["h_scale"], "saved h_scale", torch.float32, (1,))
+    dev = dout.device
+    if ws is None:
+        ws = new_mlp_workspace(T, D, F_, dev)
+    if out is None:
+        u8, bf, f = (dict(dtype=torch.uint8, device=dev), dict(dtype=torch.bfloat16, device=dev),
+                     dict(dtype=torch.float32, device=dev))
+        out = dict(dx=torch.empty((T, D), **bf), dW1=torch.empty((F_, D), **bf), dW2=torch.empty((D, F_), **bf),
+                   dout8=torch.empty((T, D), **u8), dout_scale=torch.empty((1,), **f),
+                   dpre=torch.empty((T, F_), **bf), dpre8=torch.empty((T, F_), **u8),
+                   dpre_scale=torch.empty((1,), **f))
+    o = out
+    for name, dt, shp in (("dx", torch.bfloat16, (T, D)), ("dW1", torch.bfloat16, (F_, D)),
+                          ("dW2", torch.bfloat16, (D, F_)), ("dout8", torch.uint8, (T, D)),
+                          ("dout_scale", torch.float32, (1,)), ("dpre", torch.bfloat16, (T, F_)),
+                          ("dpre8", torch.uint8, (T, F_)), ("dpre_scale", torch.float32, (1,))):
+        _need_cuda(o[name], name, dt, shp)
+    _check(lib().qkvp_mlp_backward(T, D, F_, _ptr(dout), _ptr(W1_8T), _ptr(w1_scale), _ptr(W2_8T), _ptr(w2_scale),
+                                   _ptr(saved["x8"]), _ptr(saved["x_scale"]), _ptr(saved["h8"]),
+                                   _ptr(saved["h_scale"]), _ptr(o["dx"]), _ptr(o["dW1"]), _ptr(o["dW2"]),
+                                   _ptr(o["dout8"]), _ptr(o["dout_scale"]), _ptr(o["dpre"]), _ptr(o["dpre8"]),
+                                   _ptr(o["dpre_scale"]), _ptr(ws), ws.numel(), _stream(dev)), "qkvp_mlp_backward")
     return o

@@ -179,10 +179,13 @@ int quantize_activation(const uint16_t* x, int64_t n, uint8_t* x8, float* parts,
   return QKVP_OK;
 }
 
-// out [T, Nout] bf16 = (A8 [T, K] . B8 [Nout, K]^T) * sa * sb, both operands
-// K-major codes (the dX GEMM body).  K and Nout multiples of 128.
+// out [T, Nout] bf16 = epilogue((A8 [T, K] . B8 [Nout, K]^T) * sa * sb), both
+// operands K-major codes (the dX GEMM body).  K and Nout multiples of 128.
+// With EPI_RELU2 / EPI_DRELU2 the GEMM also writes amax partials, whose count
+// lands in *nparts.
 int gemm_nt(int T, int Nout, int K, const uint8_t* A8, const uint8_t* B8, const float* sa, const float* sb,
-            uint16_t* out, DevStatus st, int sms, cudaStream_t s) {
+            uint16_t* out, DevStatus st, int sms, cudaStream_t s, int mode = EPI_PLAIN, float* amax_parts = nullptr,
+            const uint8_t* aux8 = nullptr, const float* aux_scale = nullptr, int* nparts = nullptr) {
   const int bn = Nout % 256 == 0 ? 256 : 128;   // one box per stage: the whole B tile (this CTA's half on pairs)
   const int pair = (g_pair_mask & 2) ? 2 : 1;
   CUtensorMap tm_a, tm_b, tm_out;
@@ -201,7 +204,13 @@ int gemm_nt(int T, int Nout, int K, const uint8_t* A8, const uint8_t* B8, const 
   gp.kblocks = (K + 127) / 128;
   gp.dy_scale = sa;
   gp.w_scale = sb;
-  QKVP_TRY_CUDA(launch_dx_gemm(tm_a, tm_b, tm_out, gp, sms, st, s));
+  gp.mode = mode;
+  gp.amax_parts = amax_parts;
+  gp.aux8 = aux8;
+  gp.aux_scale = aux_scale;
+  int grid = 0;
+  QKVP_TRY_CUDA(launch_dx_gemm(tm_a, tm_b, tm_out, gp, sms, st, s, &grid));
+  if (nparts) *nparts = grid * kDxEpiWarps;
   mark(s);
   return QKVP_OK;
 }
@@ -593,6 +602,112 @@ int qkvp_oproj_backward(int T, int D, int K, const uint16_t* dout, const uint8_t
   if (rc != QKVP_OK) return rc;
   // dWo [D, K] = dout8^T . a8, both read MN-major
   return gemm_tn_split(T, D, K, ds, dout8, a8, dout_scale, a_scale, dWo, dwcount, dwparts, st, sms, s);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 ReLU-squared MLP
+// ---------------------------------------------------------------------------
+namespace {
+int check_mlp(int T, int D, int F) {
+  if (T < 1 || D < 1 || F < 1) return QKVP_ERR_INVALID_ARGUMENT;
+  if (T > (1 << 24) || D % 128 || F % 128 || D > 16384 || F > 65536) return QKVP_ERR_UNSUPPORTED;
+  return QKVP_OK;
+}
+// both weight gradients share the counters and partials (they run one after the other)
+size_t mlp_counter_bytes(int T, int D, int F) {
+  return std::max(dw_counter_bytes(dw_shape_rc(F, D, T)), dw_counter_bytes(dw_shape_rc(D, F, T)));
+}
+size_t mlp_ws_bytes(int T, int D, int F) {
+  return kStatusBytes + 2 * kPartsBytes + mlp_counter_bytes(T, D, F) +
+         std::max(dw_partial_bytes(dw_shape_rc(F, D, T), kMaxSplits), dw_partial_bytes(dw_shape_rc(D, F, T), kMaxSplits));
+}
+// h, dpre: bf16 intermediates quantised from the GEMM's own amax partials
+int quantize_from_parts(const uint16_t* v, int64_t n, uint8_t* v8, const float* parts, int nparts, float* scale,
+                        int sms, cudaStream_t s) {
+  if (nparts < 1 || nparts > kMaxParts) return QKVP_ERR_CUDA;
+  QKVP_TRY_CUDA(launch_x_quant(v, n, v8, parts, nparts, scale, 4 * sms, s));
+  mark(s);
+  return QKVP_OK;
+}
+}  // namespace
+
+size_t qkvp_mlp_workspace_bytes(int T, int D, int F) {
+  if (check_mlp(T, D, F) != QKVP_OK) return 0;
+  return mlp_ws_bytes(T, D, F);
+}
+
+int qkvp_mlp_forward(int T, int D, int F, const uint16_t* x, const uint8_t* W1_8, const float* w1_scale,
+                     const uint8_t* W2_8, const float* w2_scale, uint16_t* out, uint8_t* x8, float* x_scale,
+                     uint16_t* h, uint8_t* h8, float* h_scale, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_mlp(T, D, F);
+  if (rc != QKVP_OK) return rc;
+  if (!x || !W1_8 || !w1_scale || !W2_8 || !w2_scale || !out || !x8 || !x_scale || !h || !h8 || !h_scale || !ws)
+    return QKVP_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {x, W1_8, w1_scale, W2_8, w2_scale, out, x8, x_scale, h, h8, h_scale, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < mlp_ws_bytes(T, D, F)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return QKVP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* parts_a = reinterpret_cast<float*>(wsb + kStatusBytes);
+  float* parts_b = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
+  const DevStatus st = dev_status(ws);
+  rc = quantize_activation(x, static_cast<int64_t>(T) * D, x8, parts_a, x_scale, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // h [T, F] = relu(x8 . W1_8^T * s_x * s_1)^2 in bf16, with its amax partials
+  int nparts = 0;
+  rc = gemm_nt(T, F, D, x8, W1_8, x_scale, w1_scale, h, st, sms, s, EPI_RELU2, parts_b, nullptr, nullptr, &nparts);
+  if (rc != QKVP_OK) return rc;
+  rc = quantize_from_parts(h, static_cast<int64_t>(T) * F, h8, parts_b, nparts, h_scale, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // out [T, D] = h8 . W2_8^T * s_h * s_2
+  return gemm_nt(T, D, F, h8, W2_8, h_scale, w2_scale, out, st, sms, s);
+}
+
+int qkvp_mlp_backward(int T, int D, int F, const uint16_t* dout, const uint8_t* W1_8T, const float* w1_scale,
+                      const uint8_t* W2_8T, const float* w2_scale, const uint8_t* x8, const float* x_scale,
+                      const uint8_t* h8, const float* h_scale, uint16_t* dx, uint16_t* dW1, uint16_t* dW2,
+                      uint8_t* dout8, float* dout_scale, uint16_t* dpre, uint8_t* dpre8, float* dpre_scale, void* ws,
+                      size_t ws_bytes, void* stream) {
+  int rc = check_mlp(T, D, F);
+  if (rc != QKVP_OK) return rc;
+  if (!dout || !W1_8T || !w1_scale || !W2_8T || !w2_scale || !x8 || !x_scale || !h8 || !h_scale || !dx || !dW1 ||
+      !dW2 || !dout8 || !dout_scale || !dpre || !dpre8 || !dpre_scale || !ws)
+    return QKVP_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {dout, W1_8T, w1_scale, W2_8T, w2_scale, x8, x_scale, h8, h_scale, dx, dW1, dW2, dout8,
+                        dout_scale, dpre, dpre8, dpre_scale, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < mlp_ws_bytes(T, D, F)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return QKVP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* parts_a = reinterpret_cast<float*>(wsb + kStatusBytes);
+  float* parts_b = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
+  int* dwcount = reinterpret_cast<int*>(wsb + kStatusBytes + 2 * kPartsBytes);
+  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes + mlp_counter_bytes(T, D, F));
+  const DevStatus st = dev_status(ws);
+  rc = quantize_activation(dout, static_cast<int64_t>(T) * D, dout8, parts_a, dout_scale, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // dpre [T, F] = (dout8 . W2_8 * s_g * s_2) * 2 sqrt(h8 * s_h), via the cached W2_8T [F, D]
+  int nparts = 0;
+  rc = gemm_nt(T, F, D, dout8, W2_8T, dout_scale, w2_scale, dpre, st, sms, s, EPI_DRELU2, parts_b, h8, h_scale,
+               &nparts);
+  if (rc != QKVP_OK) return rc;
+  rc = quantize_from_parts(dpre, static_cast<int64_t>(T) * F, dpre8, parts_b, nparts, dpre_scale, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // dx [T, D] = dpre8 . W1_8 * s_p * s_1, via the cached W1_8T [D, F]
+  rc = gemm_nt(T, D, F, dpre8, W1_8T, dpre_scale, w1_scale, dx, st, sms, s);
+  if (rc != QKVP_OK) return rc;
+  // dW1 [F, D] = dpre8^T . x8;  dW2 [D, F] = dout8^T . h8  (both operands MN-major)
+  rc = gemm_tn_split(T, F, D, dw_shape_rc(F, D, T), dpre8, x8, dpre_scale, x_scale, dW1, dwcount, dwparts, st, sms,
+                     s);
+  if (rc != QKVP_OK) return rc;
+  return gemm_tn_split(T, D, F, dw_shape_rc(D, F, T), dout8, h8, dout_scale, h_scale, dW2, dwcount, dwparts, st,
+                       sms, s);
 }
 
 }  // extern "C"

@@ -492,7 +492,7 @@ struct FwdEpi {
 };
 
 // Epilogue warps and per-warp staging bytes of each GEMM.
-constexpr int kFwdEW = 8, kDxEW = 4, kDwEW = kDwEpiWarps;
+constexpr int kFwdEW = 8, kDxEW = kDxEpiWarps, kDwEW = kDwEpiWarps;
 constexpr int kFwdEPB = 8192, kDxEPB = 8192;
 
 template <int DQK, bool PAIR>
@@ -537,6 +537,21 @@ struct DxSched {
   }
 };
 
+// Eight E4M3 codes (a 64-bit word, lowest byte first) as floats.
+__device__ __forceinline__ void decode8(uint2 w, float* out) {
+  const uint32_t u[2] = {w.x, w.y};
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[k] >> (16 * h)), __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      out[4 * k + 2 * h] = f.x;
+      out[4 * k + 2 * h + 1] = f.y;
+    }
+}
+
+template <int MODE>
 struct DxEpi {
   const DxParams& p;
   const DxSched& sc;
@@ -544,6 +559,8 @@ struct DxEpi {
   uint8_t* stage;
   int qw, sub, nsub, lane, ring;
   float scl;   // s_dy * s_w
+  float sh;    // DRELU2: scale of the stored codes
+  float mx;    // RELU2 / DRELU2: running max |output| of this thread
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t* stage_) {
     qw = qw_;
     sub = sub_;
@@ -552,10 +569,17 @@ struct DxEpi {
     stage = stage_;
     ring = 0;
     scl = (*p.dy_scale) * (*p.w_scale);
+    sh = MODE == EPI_DRELU2 ? *p.aux_scale : 0.f;
+    mx = 0.f;
   }
   __device__ void finish() {
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
+    if (MODE != EPI_PLAIN) {
+      // rounding is monotone, so the bf16 of the max is the max of the bf16 outputs
+      const float m = __bfloat162float(__float2bfloat16_rn(warp_max(mx)));
+      if (lane == 0) p.amax_parts[blockIdx.x * kDxEpiWarps + qw + 4 * sub] = m;
+    }
   }
   __device__ void prepare(int) {}
   __device__ void post(int) {}
@@ -567,17 +591,47 @@ struct DxEpi {
       uint8_t* slot = stage + (ring & 3) * 2048;
       if (lane == 0) bulk_wait_read<3>();
       __syncwarp();
+      uint4 hc[2];   // DRELU2: this row's 32 stored codes, in flight during the TMEM load
+      if (MODE == EPI_DRELU2) {
+        hc[0] = hc[1] = make_uint4(0, 0, 0, 0);
+        if (ty + lane < p.T) {
+          const uint4* src =
+              reinterpret_cast<const uint4*>(p.aux8 + static_cast<int64_t>(ty + lane) * p.D + j * p.bn + c0);
+          hc[0] = __ldg(src);
+          hc[1] = __ldg(src + 1);
+        }
+      }
       uint32_t raw[32];
       tmem_ld16(tacc + c0, raw);
       tmem_ld16(tacc + c0 + 16, raw + 16);
       tmem_ld_wait();
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]) * scl;
+      if (MODE == EPI_RELU2) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float r = fmaxf(v[i], 0.f);
+          v[i] = r * r;
+          mx = fmaxf(mx, v[i]);
+        }
+      } else if (MODE == EPI_DRELU2) {
+        float hv[32];
+        decode8(make_uint2(hc[0].x, hc[0].y), hv);
+        decode8(make_uint2(hc[0].z, hc[0].w), hv + 8);
+        decode8(make_uint2(hc[1].x, hc[1].y), hv + 16);
+        decode8(make_uint2(hc[1].z, hc[1].w), hv + 24);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = v[i] * (2.f * sqrtf(hv[i] * sh));
+          mx = fmaxf(mx, fabsf(v[i]));
+        }
+      }
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
         uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(raw[g * 16 + 2 * i]) * scl,
-                             __uint_as_float(raw[g * 16 + 2 * i + 1]) * scl);
+        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[g * 16 + 2 * i], v[g * 16 + 2 * i + 1]);
         stage16(slot, lane, g * 16, w);
       }
       fence_async_smem();
@@ -591,13 +645,13 @@ struct DxEpi {
   }
 };
 
-template <bool PAIR>
+template <bool PAIR, int MODE>
 __global__ void __launch_bounds__(gemm_threads(kDxEW), 1)
     dx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tdx, const __grid_constant__ DxParams p, DevStatus st,
                    Ring ring) {
   DxSched sc{p, PAIR ? static_cast<int>(cluster_rank()) : 0, PAIR ? 2 : 1};
-  DxEpi epi{p, sc, &tdx};
+  DxEpi<MODE> epi{p, sc, &tdx};
   gemm_body<kDxEW, kDxEPB, PAIR>(sc, epi, &tmA, &tmB, ring, st, KID_DX_GEMM);
 }
 
@@ -778,7 +832,7 @@ struct ClusterCache {
 // 2-CTA cluster per co-resident pair of SMs (at most one per unit).
 template <class... KArgs, class... Args>
 static cudaError_t launch_persistent(void (*kernel)(KArgs...), bool pair, int units, int sms, int threads, int smem,
-                                     ClusterCache& cache, cudaStream_t s, Args&&... args) {
+                                     ClusterCache& cache, int* grid_used, cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(threads);
@@ -809,6 +863,7 @@ static cudaError_t launch_persistent(void (*kernel)(KArgs...), bool pair, int un
     grid = 2 * (units < clusters ? units : clusters);
   }
   cfg.gridDim = dim3(grid);
+  if (grid_used) *grid_used = grid;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -824,7 +879,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, 
   cudaError_t e = set_smem_once(fwd_gemm_kernel<DQK, PAIR>, done);
   if (e != cudaSuccess) return e;
   return launch_persistent(fwd_gemm_kernel<DQK, PAIR>, PAIR, p.num_units, sms, gemm_threads(kFwdEW),
-                           gemm_smem_bytes(ring, kFwdEW, kFwdEPB), cache, s, tmA, tmB, tmBv, tq, tk, tv, p, st,
+                           gemm_smem_bytes(ring, kFwdEW, kFwdEPB), cache, nullptr, s, tmA, tmB, tmBv, tq, tk, tv, p, st,
                            ring);
 }
 
@@ -847,21 +902,33 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
                      : launch_fwd_p<false>(tmA, tmB, tmBv, tq, tk, tv, p, sms, st, s);
 }
 
-template <bool PAIR>
+template <bool PAIR, int MODE>
 static cudaError_t launch_dx_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
-                               const DxParams& p, int sms, DevStatus st, cudaStream_t s) {
+                               const DxParams& p, int sms, DevStatus st, cudaStream_t s, int* grid_used) {
   static bool done[64] = {};
   static ClusterCache cache;
   const Ring ring = ring_for(p.bn / p.pair * kBK, kDxEW, kDxEPB);
-  cudaError_t e = set_smem_once(dx_gemm_kernel<PAIR>, done);
+  cudaError_t e = set_smem_once(dx_gemm_kernel<PAIR, MODE>, done);
   if (e != cudaSuccess) return e;
-  return launch_persistent(dx_gemm_kernel<PAIR>, PAIR, p.num_units, sms, gemm_threads(kDxEW),
-                           gemm_smem_bytes(ring, kDxEW, kDxEPB), cache, s, tmA, tmB, tdx, p, st, ring);
+  return launch_persistent(dx_gemm_kernel<PAIR, MODE>, PAIR, p.num_units, sms, gemm_threads(kDxEW),
+                           gemm_smem_bytes(ring, kDxEW, kDxEPB), cache, grid_used, s, tmA, tmB, tdx, p, st, ring);
+}
+
+template <bool PAIR>
+static cudaError_t launch_dx_m(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
+                               const DxParams& p, int sms, DevStatus st, cudaStream_t s, int* grid_used) {
+  switch (p.mode) {
+    case EPI_PLAIN: return launch_dx_t<PAIR, EPI_PLAIN>(tmA, tmB, tdx, p, sms, st, s, grid_used);
+    case EPI_RELU2: return launch_dx_t<PAIR, EPI_RELU2>(tmA, tmB, tdx, p, sms, st, s, grid_used);
+    case EPI_DRELU2: return launch_dx_t<PAIR, EPI_DRELU2>(tmA, tmB, tdx, p, sms, st, s, grid_used);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
-                           const DxParams& p, int sms, DevStatus st, cudaStream_t s) {
-  return p.pair == 2 ? launch_dx_t<true>(tmA, tmB, tdx, p, sms, st, s) : launch_dx_t<false>(tmA, tmB, tdx, p, sms, st, s);
+                           const DxParams& p, int sms, DevStatus st, cudaStream_t s, int* grid_used) {
+  return p.pair == 2 ? launch_dx_m<true>(tmA, tmB, tdx, p, sms, st, s, grid_used)
+                     : launch_dx_m<false>(tmA, tmB, tdx, p, sms, st, s, grid_used);
 }
 
 template <bool PAIR>
@@ -873,7 +940,7 @@ static cudaError_t launch_dw_t(const CUtensorMap& tmA, const CUtensorMap& tmB, c
   cudaError_t e = set_smem_once(dw_gemm_kernel<PAIR>, done);
   if (e != cudaSuccess) return e;
   return launch_persistent(dw_gemm_kernel<PAIR>, PAIR, p.num_units, sms, gemm_threads(kDwEW),
-                           gemm_smem_bytes(ring, kDwEW, 0), cache, s, tmA, tmB, p, st, ring);
+                           gemm_smem_bytes(ring, kDwEW, 0), cache, nullptr, s, tmA, tmB, p, st, ring);
 }
 
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,

@@ -60,14 +60,30 @@ struct FwdParams {
   float* rstd;        // [2, H, T]
 };
 
+// Epilogues of the dX-shaped GEMM (out = A . B^T * sa * sb, bf16):
+//   EPI_PLAIN   the scaled product
+//   EPI_RELU2   relu(v)^2 of the scaled product v, plus per-warp amax partials
+//   EPI_DRELU2  v * 2 sqrt(h^) with h^ the de-quantised codes aux8 (same
+//               [T, D] layout as the output) times aux_scale, plus per-warp
+//               amax partials (the ReLU-squared backward, relu(pre) rebuilt
+//               from the stored squared activation)
+enum EpiMode : int { EPI_PLAIN = 0, EPI_RELU2 = 1, EPI_DRELU2 = 2 };
+
 struct DxParams {
   int T, D, bn, n_tiles, pair, num_units, kblocks;   // num_units = ceil(ceil(T/128) / pair) * n_tiles
   const float* dy_scale;
   const float* w_scale;
+  int mode;                // EpiMode
+  float* amax_parts;       // RELU2 / DRELU2: [grid * 4] max |output| (bf16-rounded) per CTA and epilogue warp
+  const uint8_t* aux8;     // DRELU2: [T, D] E4M3 codes
+  const float* aux_scale;  // DRELU2: their scale
 };
 
 // Epilogue warps of the dW GEMM; each owns one counter per output tile.
 constexpr int kDwEpiWarps = 8;
+// Epilogue warps of the dX-shaped GEMM; each writes one amax partial in the
+// RELU2 / DRELU2 modes.
+constexpr int kDxEpiWarps = 4;
 
 struct DwParams {
   // num_units = splits * ceil(m_tiles / pair) * n_tiles; kblocks_total = ceil(T/128)
@@ -85,8 +101,9 @@ struct DwParams {
 cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
                             const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                             int sms, DevStatus st, cudaStream_t s);
+// *grid_used (if non-null) receives the launch's grid (amax partials: 4 per CTA).
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
-                           const DxParams& p, int sms, DevStatus st, cudaStream_t s);
+                           const DxParams& p, int sms, DevStatus st, cudaStream_t s, int* grid_used = nullptr);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,
                            DevStatus st, cudaStream_t s);
 

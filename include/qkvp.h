@@ -282,6 +282,63 @@ int qkvp_oproj_backward(int T, int D, int K, const uint16_t* dout,
                         uint8_t* dout8, float* dout_scale,
                         void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * FP8 ReLU-squared MLP ("Track 1 ... packed FP8 attention", section
+ * "Changes": FP8 across the whole ReLU-squared forward and backward path and
+ * all of its GEMMs; the saved pre-activation is dropped, relu(pre) being
+ * recoverable from the stored squared activation):
+ *   h = relu(x . W_fc^T)^2,  out = h . W_proj^T
+ * with W_fc [F, D] and W_proj [D, F] (out x in), F the hidden width.  Weights
+ * are refreshed by qkvp_quantize_weight (both layouts).  Per-tensor E4M3
+ * scales amax/448 for x, h, dout and dpre.  h and dpre are produced in bf16
+ * by the GEMM that makes them (which also reduces their amax) and quantised
+ * from there; the backward rebuilds relu(pre) = sqrt(h^) from the stored
+ * codes h8.  Shapes: T 1 .. 2^24; D a multiple of 128 up to 16384; F a
+ * multiple of 128 up to 65536.
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of scratch qkvp_mlp_forward / qkvp_mlp_backward need (one workspace
+ * serves both; zero it once with qkvp_workspace_init, and again after a
+ * device error).  0 if the shape is unsupported. */
+size_t qkvp_mlp_workspace_bytes(int T, int D, int F);
+
+/* Forward:
+ *   x        in  [T, D] bf16
+ *   W1_8     in  [F, D] codes of W_fc, w1_scale [1]
+ *   W2_8     in  [D, F] codes of W_proj, w2_scale [1]
+ *   out      out [T, D] bf16
+ *   x8       out [T, D] codes, x_scale [1]           (saved for the backward)
+ *   h        out [T, F] bf16 squared activation (an intermediate; may be
+ *                reused by the caller once the call has run, e.g. as dpre)
+ *   h8       out [T, F] codes, h_scale [1]           (saved for the backward) */
+int qkvp_mlp_forward(int T, int D, int F, const uint16_t* x,
+                     const uint8_t* W1_8, const float* w1_scale,
+                     const uint8_t* W2_8, const float* w2_scale,
+                     uint16_t* out, uint8_t* x8, float* x_scale,
+                     uint16_t* h, uint8_t* h8, float* h_scale,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* Backward:
+ *   dout     in  [T, D] bf16
+ *   W1_8T    in  [D, F] codes (W_fc transposed), w1_scale [1]
+ *   W2_8T    in  [F, D] codes (W_proj transposed), w2_scale [1]
+ *   x8, h8   in  the forward's saved codes and scales
+ *   dx       out [T, D] bf16      = dpre^ . W_fc^
+ *   dW1      out [F, D] bf16      = dpre^^T . x^   (split over tokens, fixed order)
+ *   dW2      out [D, F] bf16      = dout^^T . h^   (split over tokens, fixed order)
+ *   dout8    out [T, D] codes, dout_scale [1]
+ *   dpre     out [T, F] bf16      = (dout^ . W_proj^) * 2 sqrt(h^) (intermediate)
+ *   dpre8    out [T, F] codes, dpre_scale [1]                              */
+int qkvp_mlp_backward(int T, int D, int F, const uint16_t* dout,
+                      const uint8_t* W1_8T, const float* w1_scale,
+                      const uint8_t* W2_8T, const float* w2_scale,
+                      const uint8_t* x8, const float* x_scale,
+                      const uint8_t* h8, const float* h_scale,
+                      uint16_t* dx, uint16_t* dW1, uint16_t* dW2,
+                      uint8_t* dout8, float* dout_scale,
+                      uint16_t* dpre, uint8_t* dpre8, float* dpre_scale,
+                      void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

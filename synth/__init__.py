@@ -106,6 +106,16 @@ def oproj_inputs(T: int, D: int, K: int, seed: int = 0, device="cpu"):
                 dout=_normal((T, D), 1.0, seed + 22, device))
 
 
+def mlp_inputs(T: int, D: int, F: int, seed: int = 0, device="cpu"):
+    """ReLU-squared MLP: x [T, D] ~ N(0, 1), W_fc [F, D] ~ N(0, 1/D), W_proj
+    [D, F] ~ N(0, 1/F) (fan-in scaling) and dout [T, D] ~ N(0, 1), all bf16;
+    generators seeded seed+30 ... seed+33."""
+    return dict(x=_normal((T, D), 1.0, seed + 30, device),
+                W1=_normal((F, D), D ** -0.5, seed + 31, device),
+                W2=_normal((D, F), F ** -0.5, seed + 32, device),
+                dout=_normal((T, D), 1.0, seed + 33, device))
+
+
 def to_numpy_f32(t: torch.Tensor):
     """bf16/float tensor -> float32 NumPy array holding the same values."""
     return t.detach().to("cpu", torch.float32).numpy()

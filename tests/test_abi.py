@@ -151,6 +151,25 @@ def test_oproj_validation_codes(qk):
     assert qw(1, 768, 768, arr, p, p, p, p, 8, None) == qk.ERR_WORKSPACE_TOO_SMALL
 
 
+def test_mlp_validation_codes(qk):
+    lib = qk.lib()
+    p = ctypes.c_void_p(4096)
+    assert lib.qkvp_mlp_workspace_bytes(128, 768, 3072) > 0
+    assert lib.qkvp_mlp_workspace_bytes(128, 768, 3000) == 0
+    fwd = lib.qkvp_mlp_forward
+    args = [p] * 11
+    assert fwd(0, 768, 3072, *args, p, 1 << 40, None) == qk.ERR_INVALID_ARGUMENT
+    assert fwd(128, 768, 3000, *args, p, 1 << 40, None) == qk.ERR_UNSUPPORTED
+    assert fwd(128, 768, 3072, *args, None, 1 << 40, None) == qk.ERR_INVALID_ARGUMENT
+    assert fwd(128, 768, 3072, ctypes.c_void_p(4104), *args[1:], p, 1 << 40, None) == qk.ERR_MISALIGNED
+    assert fwd(128, 768, 3072, *args, p, 64, None) == qk.ERR_WORKSPACE_TOO_SMALL
+    bwd = lib.qkvp_mlp_backward
+    bargs = [p] * 17
+    assert bwd(128, 700, 3072, *bargs, p, 1 << 40, None) == qk.ERR_UNSUPPORTED
+    assert bwd(128, 768, 3072, *bargs, None, 1 << 40, None) == qk.ERR_INVALID_ARGUMENT
+    assert bwd(128, 768, 3072, *bargs, p, 64, None) == qk.ERR_WORKSPACE_TOO_SMALL
+
+
 def test_product_path_refuses_without_library(tmp_path, monkeypatch):
     import fp8_packed_reduced_gb300 as pkg
     monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "missing.so"))

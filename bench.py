@@ -330,11 +330,56 @@ def run_ours(args, rank, world):
         "launch": "the K timed steps replayed as one captured CUDA graph",
         "clocks": clocks, "e2e": e2e,
     }
-    if not args.no_oproj:
-        line["next_rows"] = {"oproj": run_oproj(args, dev, world)}
+    if not args.no_next_rows:
+        line["next_rows"] = {"oproj": run_oproj(args, dev, world), "mlp": run_mlp(args, dev, world)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, args.cpu_sample)
     return line
+
+
+def time_in_graph(step, n_events, steps, warmup, dev, world, ws_list):
+    """Run `step` warmup times, capture `steps` calls in one CUDA graph with
+    the library's kernel-boundary events (n_events per call) and replay it
+    once untimed and once timed.  Returns (ms per step, max over ranks; list
+    of per-call event lists)."""
+    import fp8_packed_reduced_gb300 as qk
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(steps)]
+    for ev in events:
+        for e in ev:
+            e.record(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(steps):
+            qk.set_timing_events(events[i])
+            step()
+        qk.set_timing_events([])
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1) / steps, world, dev)
+    for ws in ws_list:
+        code, where = qk.poll_device_status(ws)
+        if code != 0:
+            raise RuntimeError(f"device status {qk.STATUS.get(code)} from kernel {where}")
+    return ms, events
+
+
+def span_means(events, kernels, spans):
+    per = {k: 0.0 for k in kernels}
+    for ev in events:
+        for name, (a, b_) in zip(kernels, spans):
+            per[name] += ev[a].elapsed_time(ev[b_]) / len(events)
+    return per
 
 
 OPROJ_KERNELS = ["w_amax", "w_quant", "a_amax", "a_quant", "out_gemm", "g_amax", "g_quant", "da_gemm", "dwo_gemm"]
@@ -363,37 +408,8 @@ def run_oproj(args, dev, world):
         qk.oproj_backward(inp["dout"], W8T[0], so[0:1], a8, sa, ws=ws, out=bo)
 
     steps = max(3, min(args.steps, 100))
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(OPROJ_EVENTS)] for _ in range(steps)]
-    stream = torch.cuda.current_stream(dev)
-    for ev in events:
-        for e in ev:
-            e.record(stream)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for i in range(steps):
-            qk.set_timing_events(events[i])
-            step()
-        qk.set_timing_events([])
-    torch.cuda.synchronize()
-    graph.replay()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    graph.replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(t0.elapsed_time(t1) / steps, world, dev)
-    code, where = qk.poll_device_status(ws)
-    if code != 0:
-        raise RuntimeError(f"device status {qk.STATUS.get(code)} from kernel {where}")
-    per = {k: 0.0 for k in OPROJ_KERNELS}
-    for ev in events:
-        for name, (a, b_) in zip(OPROJ_KERNELS, OPROJ_SPANS):
-            per[name] += ev[a].elapsed_time(ev[b_]) / steps
+    ms, events = time_in_graph(step, OPROJ_EVENTS, steps, args.warmup, dev, world, [ws])
+    per = span_means(events, OPROJ_KERNELS, OPROJ_SPANS)
     flops = 2.0 * T * D * K
     work = {"w_amax": ("hbm", D * K * 2), "w_quant": ("hbm", D * K * 4), "a_amax": ("hbm", T * K * 2),
             "a_quant": ("hbm", T * K * 3), "out_gemm": ("tensor", flops), "g_amax": ("hbm", T * D * 2),
@@ -403,6 +419,51 @@ def run_oproj(args, dev, world):
                         "weight refresh per step",
             "value": round(job_tokens_per_s(T, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
             "steps": steps, "kernels": kern, "gpu_launches": len(OPROJ_KERNELS) * steps}
+
+
+MLP_KERNELS = ["w1_amax", "w1_quant", "w2_amax", "w2_quant", "x_amax", "x_quant", "fc_gemm", "h_quant",
+               "proj_gemm", "g_amax", "g_quant", "dh_gemm", "dpre_quant", "dx_gemm", "dw1_gemm", "dw2_gemm"]
+MLP_SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (6, 7), (7, 8), (8, 9), (9, 10), (10, 11), (12, 13), (13, 14),
+             (14, 15), (15, 16), (16, 17), (17, 18), (18, 19)]
+MLP_EVENTS = 20
+
+
+def run_mlp(args, dev, world):
+    """The FP8 ReLU-squared MLP (both weight refreshes + forward + backward) on
+    the same token count, hidden width F = 4 D, timed like the main step."""
+    import fp8_packed_reduced_gb300 as qk
+    T, D = args.T, args.D
+    F_ = 4 * D
+    inp = synth.mlp_inputs(T, D, F_, seed=0, device=dev)
+    u8, f = dict(dtype=torch.uint8, device=dev), dict(dtype=torch.float32, device=dev)
+    w1 = (torch.empty((1, F_, D), **u8), torch.empty((1, D, F_), **u8), torch.empty((1,), **f))
+    w2 = (torch.empty((1, D, F_), **u8), torch.empty((1, F_, D), **u8), torch.empty((1,), **f))
+    ws = qk.new_mlp_workspace(T, D, F_, dev)
+    W1_8, W1_8T, s1 = qk.quantize_weight([inp["W1"]], out=w1)
+    W2_8, W2_8T, s2 = qk.quantize_weight([inp["W2"]], out=w2)
+    fo = qk.mlp_forward(inp["x"], W1_8[0], s1[0:1], W2_8[0], s2[0:1], ws=ws)
+    bo = qk.mlp_backward(inp["dout"], W1_8T[0], s1[0:1], W2_8T[0], s2[0:1], fo, ws=ws)
+
+    def step():
+        qk.quantize_weight([inp["W1"]], out=w1)
+        qk.quantize_weight([inp["W2"]], out=w2)
+        qk.mlp_forward(inp["x"], W1_8[0], s1[0:1], W2_8[0], s2[0:1], ws=ws, out=fo)
+        qk.mlp_backward(inp["dout"], W1_8T[0], s1[0:1], W2_8T[0], s2[0:1], fo, ws=ws, out=bo)
+
+    steps = max(3, min(args.steps, 50))
+    ms, events = time_in_graph(step, MLP_EVENTS, steps, args.warmup, dev, world, [ws])
+    per = span_means(events, MLP_KERNELS, MLP_SPANS)
+    fl = 2.0 * T * D * F_
+    work = {"w1_amax": ("hbm", F_ * D * 2), "w1_quant": ("hbm", F_ * D * 4), "w2_amax": ("hbm", F_ * D * 2),
+            "w2_quant": ("hbm", F_ * D * 4), "x_amax": ("hbm", T * D * 2), "x_quant": ("hbm", T * D * 3),
+            "fc_gemm": ("tensor", fl), "h_quant": ("hbm", T * F_ * 3), "proj_gemm": ("tensor", fl),
+            "g_amax": ("hbm", T * D * 2), "g_quant": ("hbm", T * D * 3), "dh_gemm": ("tensor", fl),
+            "dpre_quant": ("hbm", T * F_ * 3), "dx_gemm": ("tensor", fl), "dw1_gemm": ("tensor", fl),
+            "dw2_gemm": ("tensor", fl)}
+    kern = kernel_table(per, work, load_peaks())
+    return {"workload": f"FP8 ReLU-squared MLP fwd+bwd, T={T}, D={D}, F={F_}, both weight refreshes per step",
+            "value": round(job_tokens_per_s(T, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+            "steps": steps, "kernels": kern, "gpu_launches": len(MLP_KERNELS) * steps}
 
 
 def run_e2e(st: Step, args, dev, world):
@@ -513,7 +574,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=8192, help="tokens the oracle times for cpu_baseline")
     ap.add_argument("--ref-sample", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-oproj", action="store_true", help="skip the output-projection measurement")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the output-projection and MLP measurements")
     ap.add_argument("--cta-pairs", type=int, default=None,
                     help="GEMMs on 2-CTA clusters: bit 0 forward, bit 1 dX, bit 2 dW (default: the library's)")
     args = ap.parse_args()

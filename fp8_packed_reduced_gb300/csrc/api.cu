@@ -210,7 +210,7 @@ int gemm_nt(int T, int Nout, int K, const uint8_t* A8, const uint8_t* B8, const 
   gp.aux_scale = aux_scale;
   int grid = 0;
   QKVP_TRY_CUDA(launch_dx_gemm(tm_a, tm_b, tm_out, gp, sms, st, s, &grid));
-  if (nparts) *nparts = grid * kDxEpiWarps;
+  if (nparts) *nparts = grid * dx_epi_warps(mode);
   mark(s);
   return QKVP_OK;
 }

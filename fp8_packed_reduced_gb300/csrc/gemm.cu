@@ -492,7 +492,7 @@ struct FwdEpi {
 };
 
 // Epilogue warps and per-warp staging bytes of each GEMM.
-constexpr int kFwdEW = 8, kDxEW = kDxEpiWarps, kDwEW = kDwEpiWarps;
+constexpr int kFwdEW = 8, kDwEW = kDwEpiWarps;
 constexpr int kFwdEPB = 8192, kDxEPB = 8192;
 
 template <int DQK, bool PAIR>
@@ -537,20 +537,6 @@ struct DxSched {
   }
 };
 
-// Eight E4M3 codes (a 64-bit word, lowest byte first) as floats.
-__device__ __forceinline__ void decode8(uint2 w, float* out) {
-  const uint32_t u[2] = {w.x, w.y};
-#pragma unroll
-  for (int k = 0; k < 2; ++k)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[k] >> (16 * h)), __NV_E4M3);
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-      out[4 * k + 2 * h] = f.x;
-      out[4 * k + 2 * h + 1] = f.y;
-    }
-}
-
 template <int MODE>
 struct DxEpi {
   const DxParams& p;
@@ -559,8 +545,13 @@ struct DxEpi {
   uint8_t* stage;
   int qw, sub, nsub, lane, ring;
   float scl;   // s_dy * s_w
-  float sh;    // DRELU2: scale of the stored codes
+  float k2;    // DRELU2: 2 sqrt(scale of the stored codes)
   float mx;    // RELU2 / DRELU2: running max |output| of this thread
+  const float* sqrt_tab;   // DRELU2: sqrt of the E4M3 value of each code 0 .. 127
+  // DRELU2: this thread's row of stored codes for the unit's columns (up to
+  // 256), loaded by prepare() while the accumulator is still being computed
+  static constexpr int kMaxChunks = 8;
+  uint4 hc[kMaxChunks][2];
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t* stage_) {
     qw = qw_;
     sub = sub_;
@@ -569,8 +560,24 @@ struct DxEpi {
     stage = stage_;
     ring = 0;
     scl = (*p.dy_scale) * (*p.w_scale);
-    sh = MODE == EPI_DRELU2 ? *p.aux_scale : 0.f;
     mx = 0.f;
+    if (MODE == EPI_DRELU2) {
+      // sqrt(h^) = sqrt(code value) * sqrt(s_h): the stored squared activation
+      // is non-negative, so its codes are 0 .. 0x7E and 128 square roots serve
+      __shared__ float tab[128];
+      const int i = (qw + 4 * sub) * 32 + lane;   // the epilogue warps fill the table
+      if (i < 128) {
+        float v = 0.f;
+        if (i < 0x7F) {
+          const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(i), __NV_E4M3);
+          v = sqrtf(__half2float(*reinterpret_cast<const __half*>(&hr.x)));
+        }
+        tab[i] = v;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(dx_epi_warps(MODE) * 32) : "memory");
+      sqrt_tab = tab;
+      k2 = 2.f * sqrtf(*p.aux_scale);
+    }
   }
   __device__ void finish() {
     if (lane == 0) bulk_wait_all<0>();
@@ -578,29 +585,35 @@ struct DxEpi {
     if (MODE != EPI_PLAIN) {
       // rounding is monotone, so the bf16 of the max is the max of the bf16 outputs
       const float m = __bfloat162float(__float2bfloat16_rn(warp_max(mx)));
-      if (lane == 0) p.amax_parts[blockIdx.x * kDxEpiWarps + qw + 4 * sub] = m;
+      if (lane == 0) p.amax_parts[blockIdx.x * dx_epi_warps(MODE) + qw + 4 * sub] = m;
     }
   }
-  __device__ void prepare(int) {}
+  __device__ void prepare(int u) {
+    if (MODE != EPI_DRELU2) return;
+    const int t = sc.mtile(u) * kBM + qw * 32 + lane, j = u % p.n_tiles;
+    const int share = p.bn / nsub;
+    const uint4* src = reinterpret_cast<const uint4*>(p.aux8 + static_cast<int64_t>(t) * p.D + j * p.bn + sub * share);
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+      hc[c][0] = hc[c][1] = make_uint4(0, 0, 0, 0);
+      if (t < p.T && 32 * c < share) {
+        hc[c][0] = __ldg(src + 2 * c);
+        hc[c][1] = __ldg(src + 2 * c + 1);
+      }
+    }
+  }
   __device__ void post(int) {}
   __device__ void process(int u, uint32_t tacc) {
     const int m = sc.mtile(u), j = u % p.n_tiles;
     const int ty = m * kBM + qw * 32;
     const int share = p.bn / nsub;   // this warp's columns: [sub * share, (sub + 1) * share)
-    for (int c0 = sub * share; c0 < (sub + 1) * share; c0 += 32) {
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+      if (32 * c >= share) break;
+      const int c0 = sub * share + 32 * c;
       uint8_t* slot = stage + (ring & 3) * 2048;
       if (lane == 0) bulk_wait_read<3>();
       __syncwarp();
-      uint4 hc[2];   // DRELU2: this row's 32 stored codes, in flight during the TMEM load
-      if (MODE == EPI_DRELU2) {
-        hc[0] = hc[1] = make_uint4(0, 0, 0, 0);
-        if (ty + lane < p.T) {
-          const uint4* src =
-              reinterpret_cast<const uint4*>(p.aux8 + static_cast<int64_t>(ty + lane) * p.D + j * p.bn + c0);
-          hc[0] = __ldg(src);
-          hc[1] = __ldg(src + 1);
-        }
-      }
       uint32_t raw[32];
       tmem_ld16(tacc + c0, raw);
       tmem_ld16(tacc + c0 + 16, raw + 16);
@@ -616,14 +629,11 @@ struct DxEpi {
           mx = fmaxf(mx, v[i]);
         }
       } else if (MODE == EPI_DRELU2) {
-        float hv[32];
-        decode8(make_uint2(hc[0].x, hc[0].y), hv);
-        decode8(make_uint2(hc[0].z, hc[0].w), hv + 8);
-        decode8(make_uint2(hc[1].x, hc[1].y), hv + 16);
-        decode8(make_uint2(hc[1].z, hc[1].w), hv + 24);
+        const uint32_t cw[8] = {hc[c][0].x, hc[c][0].y, hc[c][0].z, hc[c][0].w,
+                                hc[c][1].x, hc[c][1].y, hc[c][1].z, hc[c][1].w};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          v[i] = v[i] * (2.f * sqrtf(hv[i] * sh));
+          v[i] = (v[i] * k2) * sqrt_tab[(cw[i >> 2] >> (8 * (i & 3))) & 0x7Fu];
           mx = fmaxf(mx, fabsf(v[i]));
         }
       }
@@ -646,13 +656,13 @@ struct DxEpi {
 };
 
 template <bool PAIR, int MODE>
-__global__ void __launch_bounds__(gemm_threads(kDxEW), 1)
+__global__ void __launch_bounds__(gemm_threads(dx_epi_warps(MODE)), 1)
     dx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tdx, const __grid_constant__ DxParams p, DevStatus st,
                    Ring ring) {
   DxSched sc{p, PAIR ? static_cast<int>(cluster_rank()) : 0, PAIR ? 2 : 1};
   DxEpi<MODE> epi{p, sc, &tdx};
-  gemm_body<kDxEW, kDxEPB, PAIR>(sc, epi, &tmA, &tmB, ring, st, KID_DX_GEMM);
+  gemm_body<dx_epi_warps(MODE), kDxEPB, PAIR>(sc, epi, &tmA, &tmB, ring, st, KID_DX_GEMM);
 }
 
 // ---------------------------------------------------------------------------
@@ -907,11 +917,12 @@ static cudaError_t launch_dx_t(const CUtensorMap& tmA, const CUtensorMap& tmB, c
                                const DxParams& p, int sms, DevStatus st, cudaStream_t s, int* grid_used) {
   static bool done[64] = {};
   static ClusterCache cache;
-  const Ring ring = ring_for(p.bn / p.pair * kBK, kDxEW, kDxEPB);
+  constexpr int EW = dx_epi_warps(MODE);
+  const Ring ring = ring_for(p.bn / p.pair * kBK, EW, kDxEPB);
   cudaError_t e = set_smem_once(dx_gemm_kernel<PAIR, MODE>, done);
   if (e != cudaSuccess) return e;
-  return launch_persistent(dx_gemm_kernel<PAIR, MODE>, PAIR, p.num_units, sms, gemm_threads(kDxEW),
-                           gemm_smem_bytes(ring, kDxEW, kDxEPB), cache, grid_used, s, tmA, tmB, tdx, p, st, ring);
+  return launch_persistent(dx_gemm_kernel<PAIR, MODE>, PAIR, p.num_units, sms, gemm_threads(EW),
+                           gemm_smem_bytes(ring, EW, kDxEPB), cache, grid_used, s, tmA, tmB, tdx, p, st, ring);
 }
 
 template <bool PAIR>

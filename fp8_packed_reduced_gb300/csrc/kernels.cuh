@@ -74,16 +74,17 @@ struct DxParams {
   const float* dy_scale;
   const float* w_scale;
   int mode;                // EpiMode
-  float* amax_parts;       // RELU2 / DRELU2: [grid * 4] max |output| (bf16-rounded) per CTA and epilogue warp
+  float* amax_parts;       // RELU2 / DRELU2: [grid * dx_epi_warps(mode)] max |output| (bf16-rounded) per CTA and epilogue warp
   const uint8_t* aux8;     // DRELU2: [T, D] E4M3 codes
   const float* aux_scale;  // DRELU2: their scale
 };
 
 // Epilogue warps of the dW GEMM; each owns one counter per output tile.
 constexpr int kDwEpiWarps = 8;
-// Epilogue warps of the dX-shaped GEMM; each writes one amax partial in the
-// RELU2 / DRELU2 modes.
-constexpr int kDxEpiWarps = 4;
+// Epilogue warps of the dX-shaped GEMM per epilogue mode (the ReLU-squared
+// modes do more per element and take eight); each writes one amax partial in
+// the RELU2 / DRELU2 modes.
+__host__ __device__ constexpr int dx_epi_warps(int mode) { return mode == EPI_PLAIN ? 4 : 8; }
 
 struct DwParams {
   // num_units = splits * ceil(m_tiles / pair) * n_tiles; kblocks_total = ceil(T/128)
@@ -101,7 +102,8 @@ struct DwParams {
 cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
                             const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                             int sms, DevStatus st, cudaStream_t s);
-// *grid_used (if non-null) receives the launch's grid (amax partials: 4 per CTA).
+// *grid_used (if non-null) receives the launch's grid (amax partials:
+// dx_epi_warps(mode) per CTA).
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
                            const DxParams& p, int sms, DevStatus st, cudaStream_t s, int* grid_used = nullptr);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,

@@ -30,11 +30,10 @@ import torch  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "packed-QKV fwd+bwd tokens/s"
-KERNELS = ["bank_amax", "bank_quant", "x_amax", "x_quant", "fwd_gemm",
-           "dy_amax", "dy_quant", "dx_gemm", "dw_gemm"]
+KERNELS = ["bank_amax", "bank_quant", "x_quant", "fwd_gemm", "dy_amax", "dy_quant", "dx_gemm", "dw_gemm"]
 # event index pairs bracketing each kernel (see qkvp_set_timing_events)
-SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (5, 6), (7, 8), (8, 9), (9, 10), (10, 11)]
-EVENTS_PER_STEP = 12
+SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (6, 7), (7, 8), (8, 9), (9, 10)]
+EVENTS_PER_STEP = 11
 
 
 def algorithmic_work(s: synth.Shape):
@@ -49,7 +48,8 @@ def algorithmic_work(s: synth.Shape):
     return {
         "bank_amax": ("hbm", bank),
         "bank_quant": ("hbm", bank + 2 * N * D),
-        "x_amax": ("hbm", T * D * 2),
+        # amax and codes in one launch: x read (the second pass mostly from
+        # L2) and x8 written; counted once each
         "x_quant": ("hbm", T * D * 2 + T * D),
         "fwd_gemm": ("tensor", flops),
         "dy_amax": ("hbm", bwd_in),
@@ -382,9 +382,9 @@ def span_means(events, kernels, spans):
     return per
 
 
-OPROJ_KERNELS = ["w_amax", "w_quant", "a_amax", "a_quant", "out_gemm", "g_amax", "g_quant", "da_gemm", "dwo_gemm"]
-OPROJ_SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (5, 6), (7, 8), (8, 9), (9, 10), (10, 11)]
-OPROJ_EVENTS = 12
+OPROJ_KERNELS = ["w_amax", "w_quant", "a_quant", "out_gemm", "g_quant", "da_gemm", "dwo_gemm"]
+OPROJ_SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (6, 7), (7, 8), (8, 9)]
+OPROJ_EVENTS = 10
 
 
 def run_oproj(args, dev, world):
@@ -411,9 +411,9 @@ def run_oproj(args, dev, world):
     ms, events = time_in_graph(step, OPROJ_EVENTS, steps, args.warmup, dev, world, [ws])
     per = span_means(events, OPROJ_KERNELS, OPROJ_SPANS)
     flops = 2.0 * T * D * K
-    work = {"w_amax": ("hbm", D * K * 2), "w_quant": ("hbm", D * K * 4), "a_amax": ("hbm", T * K * 2),
-            "a_quant": ("hbm", T * K * 3), "out_gemm": ("tensor", flops), "g_amax": ("hbm", T * D * 2),
-            "g_quant": ("hbm", T * D * 3), "da_gemm": ("tensor", flops), "dwo_gemm": ("tensor", flops)}
+    work = {"w_amax": ("hbm", D * K * 2), "w_quant": ("hbm", D * K * 4), "a_quant": ("hbm", T * K * 3),
+            "out_gemm": ("tensor", flops), "g_quant": ("hbm", T * D * 3), "da_gemm": ("tensor", flops),
+            "dwo_gemm": ("tensor", flops)}
     kern = kernel_table(per, work, load_peaks())
     return {"workload": f"output projection over the V/O bank fwd+bwd, T={T}, D={D}, K=H*d_v={K}, "
                         "weight refresh per step",
@@ -421,11 +421,11 @@ def run_oproj(args, dev, world):
             "steps": steps, "kernels": kern, "gpu_launches": len(OPROJ_KERNELS) * steps}
 
 
-MLP_KERNELS = ["w1_amax", "w1_quant", "w2_amax", "w2_quant", "x_amax", "x_quant", "fc_gemm", "h_quant",
-               "proj_gemm", "g_amax", "g_quant", "dh_gemm", "dpre_quant", "dx_gemm", "dw1_gemm", "dw2_gemm"]
-MLP_SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (6, 7), (7, 8), (8, 9), (9, 10), (10, 11), (12, 13), (13, 14),
-             (14, 15), (15, 16), (16, 17), (17, 18), (18, 19)]
-MLP_EVENTS = 20
+MLP_KERNELS = ["w1_amax", "w1_quant", "w2_amax", "w2_quant", "x_quant", "fc_gemm", "h_quant", "proj_gemm",
+               "g_quant", "dh_gemm", "dpre_quant", "dx_gemm", "dw1_gemm", "dw2_gemm"]
+MLP_SPANS = [(0, 1), (1, 2), (3, 4), (4, 5), (6, 7), (7, 8), (8, 9), (9, 10), (11, 12), (12, 13), (13, 14),
+             (14, 15), (15, 16), (16, 17)]
+MLP_EVENTS = 18
 
 
 def run_mlp(args, dev, world):
@@ -455,9 +455,9 @@ def run_mlp(args, dev, world):
     per = span_means(events, MLP_KERNELS, MLP_SPANS)
     fl = 2.0 * T * D * F_
     work = {"w1_amax": ("hbm", F_ * D * 2), "w1_quant": ("hbm", F_ * D * 4), "w2_amax": ("hbm", F_ * D * 2),
-            "w2_quant": ("hbm", F_ * D * 4), "x_amax": ("hbm", T * D * 2), "x_quant": ("hbm", T * D * 3),
+            "w2_quant": ("hbm", F_ * D * 4), "x_quant": ("hbm", T * D * 3),
             "fc_gemm": ("tensor", fl), "h_quant": ("hbm", T * F_ * 3), "proj_gemm": ("tensor", fl),
-            "g_amax": ("hbm", T * D * 2), "g_quant": ("hbm", T * D * 3), "dh_gemm": ("tensor", fl),
+            "g_quant": ("hbm", T * D * 3), "dh_gemm": ("tensor", fl),
             "dpre_quant": ("hbm", T * F_ * 3), "dx_gemm": ("tensor", fl), "dw1_gemm": ("tensor", fl),
             "dw2_gemm": ("tensor", fl)}
     kern = kernel_table(per, work, load_peaks())

@@ -166,15 +166,18 @@ void mark(cudaStream_t s) {
     if ((expr) != cudaSuccess) return QKVP_ERR_CUDA; \
   } while (0)
 
+// The grid barrier of the fused activation quantiser, inside the status area
+// at the start of a workspace (zeroed by qkvp_workspace_init).
+GridBar* grid_bar(void* ws) { return reinterpret_cast<GridBar*>(static_cast<uint8_t*>(ws) + 128); }
+
 // Per-tensor quantisation of a bf16 activation of n elements (n % 16 == 0):
-// amax partials, then codes and the scale (two launches).
-int quantize_activation(const uint16_t* x, int64_t n, uint8_t* x8, float* parts, float* scale, int sms,
+// amax, then codes and the scale, in one launch (`parts` holds one partial per
+// block, up to kMaxFusedBlocks <= kMaxParts).
+int quantize_activation(const uint16_t* x, int64_t n, uint8_t* x8, float* parts, float* scale, void* ws,
                         cudaStream_t s) {
-  const int nparts = std::min(kMaxParts, 4 * sms);
+  static_assert(kMaxFusedBlocks <= kMaxParts, "partials buffer too small");
   mark(s);
-  QKVP_TRY_CUDA(launch_amax_bf16(x, n, parts, nparts, s));
-  mark(s);
-  QKVP_TRY_CUDA(launch_x_quant(x, n, x8, parts, nparts, scale, 4 * sms, s));
+  QKVP_TRY_CUDA(launch_x_amax_quant(x, n, x8, parts, scale, grid_bar(ws), dev_status(ws), s));
   mark(s);
   return QKVP_OK;
 }
@@ -408,7 +411,7 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return QKVP_ERR_CUDA;
 
-  rc = quantize_activation(x, static_cast<int64_t>(T) * D, x8, xparts, x_scale, sms, s);
+  rc = quantize_activation(x, static_cast<int64_t>(T) * D, x8, xparts, x_scale, ws, s);
   if (rc != QKVP_OK) return rc;
 
   FwdParams p;
@@ -569,7 +572,7 @@ int qkvp_oproj_forward(int T, int D, int K, const uint16_t* a, const uint8_t* Wo
   if (sms <= 0) return QKVP_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* aparts = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
-  rc = quantize_activation(a, static_cast<int64_t>(T) * K, a8, aparts, a_scale, sms, s);
+  rc = quantize_activation(a, static_cast<int64_t>(T) * K, a8, aparts, a_scale, ws, s);
   if (rc != QKVP_OK) return rc;
   // out [T, D] = a8 [T, K] . Wo8 [D, K]^T
   return gemm_nt(T, D, K, a8, Wo8, a_scale, wo_scale, out, dev_status(ws), sms, s);
@@ -595,7 +598,7 @@ int qkvp_oproj_backward(int T, int D, int K, const uint16_t* dout, const uint8_t
   int* dwcount = reinterpret_cast<int*>(wsb + kStatusBytes + 2 * kPartsBytes);
   float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes + dw_counter_bytes(ds));
   const DevStatus st = dev_status(ws);
-  rc = quantize_activation(dout, static_cast<int64_t>(T) * D, dout8, gparts, dout_scale, sms, s);
+  rc = quantize_activation(dout, static_cast<int64_t>(T) * D, dout8, gparts, dout_scale, ws, s);
   if (rc != QKVP_OK) return rc;
   // da [T, K] = dout8 [T, D] . Wo8 with the cached Wo8T [K, D] as the K-major operand
   rc = gemm_nt(T, K, D, dout8, Wo8T, dout_scale, wo_scale, da, st, sms, s);
@@ -654,7 +657,7 @@ int qkvp_mlp_forward(int T, int D, int F, const uint16_t* x, const uint8_t* W1_8
   float* parts_a = reinterpret_cast<float*>(wsb + kStatusBytes);
   float* parts_b = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
   const DevStatus st = dev_status(ws);
-  rc = quantize_activation(x, static_cast<int64_t>(T) * D, x8, parts_a, x_scale, sms, s);
+  rc = quantize_activation(x, static_cast<int64_t>(T) * D, x8, parts_a, x_scale, ws, s);
   if (rc != QKVP_OK) return rc;
   // h [T, F] = relu(x8 . W1_8^T * s_x * s_1)^2 in bf16, with its amax partials
   int nparts = 0;
@@ -690,7 +693,7 @@ int qkvp_mlp_backward(int T, int D, int F, const uint16_t* dout, const uint8_t* 
   int* dwcount = reinterpret_cast<int*>(wsb + kStatusBytes + 2 * kPartsBytes);
   float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes + mlp_counter_bytes(T, D, F));
   const DevStatus st = dev_status(ws);
-  rc = quantize_activation(dout, static_cast<int64_t>(T) * D, dout8, parts_a, dout_scale, sms, s);
+  rc = quantize_activation(dout, static_cast<int64_t>(T) * D, dout8, parts_a, dout_scale, ws, s);
   if (rc != QKVP_OK) return rc;
   // dpre [T, F] = (dout8 . W2_8 * s_g * s_2) * 2 sqrt(h8 * s_h), via the cached W2_8T [F, D]
   int nparts = 0;

@@ -34,6 +34,21 @@ cudaError_t launch_amax_bf16(const uint16_t* x, int64_t n, float* partials, int 
 cudaError_t launch_x_quant(const uint16_t* x, int64_t n, uint8_t* x8, const float* partials, int nparts,
                            float* x_scale, int blocks, cudaStream_t s);
 
+// A grid-wide barrier between the blocks of one launch, in device memory
+// that starts at zero and is left at zero-count after every use.
+struct GridBar {
+  int count;   // blocks arrived in the current use
+  int gen;     // uses completed (the waiters watch it change)
+};
+// Both steps in one persistent launch: amax of x (one partial per block, at
+// most kMaxFusedBlocks), a grid barrier, then every block reduces the
+// partials and quantises the same elements it read (mostly from L2 when x
+// fits there).  Every block must be resident at once: the grid is sized from
+// the occupancy of the kernel; the barrier's wait is bounded.
+constexpr int kMaxFusedBlocks = 4096;
+cudaError_t launch_x_amax_quant(const uint16_t* x, int64_t n, uint8_t* x8, float* partials, float* x_scale,
+                                GridBar* bar, DevStatus st, cudaStream_t s);
+
 cudaError_t launch_rope_table(float* table, int max_pos, int d_qk, double base, cudaStream_t s);
 cudaError_t launch_selftest_wait(DevStatus st, cudaStream_t s);
 

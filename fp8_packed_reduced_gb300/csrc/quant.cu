@@ -199,6 +199,134 @@ cudaError_t launch_x_quant(const uint16_t* x, int64_t n, uint8_t* x8, const floa
 }
 
 // ---------------------------------------------------------------------------
+// x amax and x quantise in one launch, separated by a grid barrier.
+// ---------------------------------------------------------------------------
+// Grid barrier: every block's thread 0 arrives; the last to arrive resets the
+// count and advances the generation, the others wait (bounded) for that.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void grid_barrier(GridBar* bar, const DevStatus& st, int kid) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int gen = ld_acquire_gpu(&bar->gen);
+    __threadfence();   // this block's writes before its arrival
+    if (atomicAdd(&bar->count, 1) == static_cast<int>(gridDim.x) - 1) {
+      bar->count = 0;
+      __threadfence();
+      atomicAdd(&bar->gen, 1);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(&bar->gen) == gen) {
+        if (globaltimer_ns() - t0 > st.timeout_ns) {
+          record_error(st, QKVP_ERR_TIMEOUT, kid);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+constexpr int kFusedThreads = 512;
+
+// 16-byte read-only load with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ldg_hint(const uint4* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+
+__global__ void __launch_bounds__(kFusedThreads) x_amax_quant_kernel(const uint16_t* __restrict__ x, int64_t n16,
+                                                                     uint8_t* __restrict__ x8, float* partials,
+                                                                     float* x_scale, GridBar* bar, DevStatus st) {
+  __shared__ float red[32];
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // 1: amax over this block's groups of 16 values (four groups in flight);
+  // the lines are kept in L2 with priority for step 2
+  const uint64_t keep = l2_policy_evict_last();
+  float m = 0.f;
+  int64_t i = i0;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = ldg_hint(src + 2 * (i + j * stride), keep);
+      v[2 * j + 1] = ldg_hint(src + 2 * (i + j * stride) + 1, keep);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, absmax_bf16x8(v[j]));
+  }
+  for (; i < n16; i += stride)
+    m = fmaxf(m, fmaxf(absmax_bf16x8(ldg_hint(src + 2 * i, keep)), absmax_bf16x8(ldg_hint(src + 2 * i + 1, keep))));
+  m = block_max(m, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+  grid_barrier(bar, st, KID_X_QUANT);
+  // 2: the scale from every block's partial, then the codes of the same groups
+  float pm = 0.f;   // the other blocks' partials, read from L2
+  for (int b = threadIdx.x; b < static_cast<int>(gridDim.x); b += blockDim.x) pm = fmaxf(pm, __ldcg(partials + b));
+  const float s = scale_from_amax(block_max(pm, red));
+  const Bracket k = make_bracket(s);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *x_scale = s;
+  // in the reverse order of step 1: the groups read last are the likeliest
+  // to be in L2 still
+  // (last use of the lines: they may go first)
+  const uint64_t done = l2_policy_evict_first();
+  uint4* dst = reinterpret_cast<uint4*>(x8);
+  const int64_t cnt = i0 < n16 ? (n16 - 1 - i0) / stride + 1 : 0;   // this thread's groups
+  int64_t c = cnt - 1;
+  for (; c >= 1; c -= 2) {
+    const int64_t ia = i0 + c * stride, ib = ia - stride;
+    const uint4 a0 = ldg_hint(src + 2 * ia, done), a1 = ldg_hint(src + 2 * ia + 1, done);
+    const uint4 b0 = ldg_hint(src + 2 * ib, done), b1 = ldg_hint(src + 2 * ib + 1, done);
+    dst[ia] = quant16(a0, a1, k);
+    dst[ib] = quant16(b0, b1, k);
+  }
+  if (c == 0) dst[i0] = quant16(ldg_hint(src + 2 * i0, done), ldg_hint(src + 2 * i0 + 1, done), k);
+}
+
+cudaError_t launch_x_amax_quant(const uint16_t* x, int64_t n, uint8_t* x8, float* partials, float* x_scale,
+                                GridBar* bar, DevStatus st, cudaStream_t s) {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int blocks = dev < 64 ? cache[dev] : 0;
+  if (blocks <= 0) {
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, x_amax_quant_kernel, kFusedThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    blocks = sms * per_sm < kMaxFusedBlocks ? sms * per_sm : kMaxFusedBlocks;
+    if (dev < 64) cache[dev] = blocks;
+  }
+  // no more blocks than groups of 16 values (each block then has work in both steps)
+  const int64_t n16 = n / 16;
+  const int grid = static_cast<int>(n16 < blocks ? (n16 > 0 ? n16 : 1) : blocks);
+  x_amax_quant_kernel<<<grid, kFusedThreads, 0, s>>>(x, n16, x8, partials, x_scale, bar, st);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // RoPE table, two rotation pairs per entry:
 //   table[(j * max_pos + p) * 4 + {0, 1, 2, 3}]
 //     = cos(p w_2j), cos(p w_2j+1), sin(p w_2j), sin(p w_2j+1),

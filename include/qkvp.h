@@ -209,7 +209,7 @@ int qkvp_set_wait_timeout_ns(uint64_t ns);
  * first kernel and after each kernel (as external event nodes when the stream
  * is being captured into a CUDA graph), so consecutive events bracket one
  * kernel each.  Order of the kernels: qkvp_quantize_bank: amax, quantise;
- * qkvp_forward: x amax, x quantise, forward GEMM; qkvp_backward: dY amax,
+ * qkvp_forward: x amax + quantise (one kernel), forward GEMM; qkvp_backward: dY amax,
  * dY quantise, dX GEMM, dW GEMM (with its split reduction).  n = 0 disarms.  Not
  * thread-safe; meant for benchmarks. */
 int qkvp_set_timing_events(void* const* events, int n);

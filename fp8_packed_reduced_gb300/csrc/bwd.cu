@@ -12,9 +12,10 @@
 // (RoPE is a rotation, so the inner product needs no rotation and one
 // inverse rotation of (g_out - mu * o) suffices).  dY_v = dv.
 //
-// Work unit: 128 tokens x one head x one part (q, k or v).  Persistent CTA
-// per SM of two groups of eight warps; group g takes every other unit of the
-// CTA and owns its own ring of input stages, which one of its threads refills
+// Work unit: 128 tokens x one head x one part (q, k or v); a group takes the
+// three parts of one (token tile, head) in a row, so that the k part reuses
+// the RoPE factors of the q part.  Persistent CTA per SM of two groups of
+// eight warps; each group owns its own ring of input stages, which one of its threads refills
 // by TMA (the unit's [128 tokens x 32 cols] boxes, 64-byte swizzle) as soon
 // as the group has read a stage.  Two threads per token row: thread half h
 // owns the 8-column blocks (c / 8) % 2 == h of the row, which keeps each
@@ -195,32 +196,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     inflight |= 1u << s;
     inpar = (inpar & ~(1u << s)) | (par << s);
   };
-  const int u0 = blockIdx.x + g * gridDim.x;
+  // The group's k-th unit (-1 past the end): the q, k and v parts of one
+  // (token tile, head) follow each other, the (tile, head) triples going
+  // round-robin over the grid's groups.  The k part reuses the q part's RoPE
+  // factors (same tokens, same positions).
+  const int g0 = blockIdx.x + g * gridDim.x;
+  const int ntriples = p.num_units / 3;
+  auto unit_at = [&](int k) -> int {
+    const int tr = g0 + (k / 3) * ustep;
+    return tr < ntriples ? 3 * tr + k % 3 : -1;
+  };
   if (gt == 0)
     for (int k = 0; k < SPG; ++k)
-      if (u0 + k * ustep < p.num_units) load_unit(u0 + k * ustep, k, 0);
+      if (unit_at(k) >= 0) load_unit(unit_at(k), k, 0);
 
   float mx = 0.f;
   const float4* rope = reinterpret_cast<const float4*>(p.rope);
   // the saved state of the group's next q/k unit is loaded one unit ahead
   float rstd_next = 0.f;
   int pos_next = 0;
-  if (u0 < p.num_units) {
-    const BwdUnit b0 = bwd_decode(p, u0);
+  if (unit_at(0) >= 0) {
+    const BwdUnit b0 = bwd_decode(p, unit_at(0));
     if (b0.part < 2) row_state(p, b0, b0.t0 + r, rstd_next, pos_next);
   }
-  int k = 0;
-  for (int u = u0; u < p.num_units; u += ustep, ++k) {
+  // entry w of group gg: cos, cos, sin, sin of pairs c + 2w, c + 2w + 1
+  float4 k4[NG][4];
+  for (int k = 0;; ++k) {
+    const int u = unit_at(k);
+    if (u < 0) break;
     const int s = k % SPG;
     const uint32_t par = (k / SPG) & 1;
     const BwdUnit b = bwd_decode(p, u);
     const float rstd = rstd_next;
     int pos = pos_next;
-    // this unit's RoPE factors, in flight while the stage arrives and the
-    // row's mean is formed
-    // entry w of group gg: cos, cos, sin, sin of pairs c + 2w, c + 2w + 1
-    float4 k4[NG][4];
-    if (b.part < 2) {
+    // the q part's RoPE factors, in flight while the stage arrives and the
+    // row's mean is formed (the k part that follows uses them again)
+    if (b.part == 0) {
       if (pos < 0 || pos >= p.max_pos) {
         record_error(st, QKVP_ERR_DEVICE_INPUT, kid);
         pos = 0;
@@ -232,8 +243,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int w = 0; w < 4; ++w)
           k4[gg][w] = __ldg(rope_row + static_cast<int64_t>(8 * gg + 4 * hf + w) * p.max_pos);
     }
-    if (u + ustep < p.num_units) {
-      const BwdUnit bn = bwd_decode(p, u + ustep);
+    const int un = unit_at(k + 1);
+    if (un >= 0) {
+      const BwdUnit bn = bwd_decode(p, un);
       if (bn.part < 2) row_state(p, bn, bn.t0 + r, rstd_next, pos_next);
     }
     if (!group_all(g, mbar_wait(&gfull[s], par, &abort_flag, st, kid))) break;
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (QUANT) fence_async_smem();
       // every value read from the stage has been used by now (see the v path)
       group_sync_after(g, mx);   // the stage is read (and, in pass 2, the codes are staged)
-      if (gt == 0 && u + SPG * ustep < p.num_units) load_unit(u + SPG * ustep, s, par ^ 1u);
+      if (gt == 0 && unit_at(k + SPG) >= 0) load_unit(unit_at(k + SPG), s, par ^ 1u);
     } else {
       uint4 x[8];
 #pragma unroll
@@ -318,7 +330,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mx = fmax3(mx, bf16_lo(m2), bf16_hi(m2));
       }
       group_sync_after(g, mx);   // the stage is read (and, in pass 2, the codes are staged)
-      if (gt == 0 && u + SPG * ustep < p.num_units) load_unit(u + SPG * ustep, s, par ^ 1u);
+      if (gt == 0 && unit_at(k + SPG) >= 0) load_unit(unit_at(k + SPG), s, par ^ 1u);
       nbox = 4;
     }
     if (QUANT && gt == 0) {

@@ -67,9 +67,9 @@ def algorithmic_work(s: synth.Shape):
 KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu"}
 TRAFFIC = {
     "T": 24576,
-    "sources_sha256": {"bwd": "5cddaa41ab74c2ce6464ba9ac423bbc2b9e9d1d0ac201d9dfe2a9356cfedc022", "gemm": "4402b4c9e7e3d5472575b4a8b29698e6023b08771c5b49bc6fa180182fab8d00"},
-    "bytes": {"dy_amax": ("bwd", 159.37e6), "dy_quant": ("bwd", 181.00e6), "fwd_gemm": ("gemm", 64.65e6),
-              "dx_gemm": ("gemm", 52.55e6), "dw_gemm": ("gemm", 69.47e6)},
+    "sources_sha256": {"bwd": "b3d41929d5febd1d9aa415f5d94aacbf89ecc8b6e494d96761e6af9b37a04e94", "gemm": "d6d7da1af52f2674366ae814ad5dbe89eb640ab0c99ccf6ee711b0ddffea7007"},
+    "bytes": {"dy_amax": ("bwd", 159.09e6), "dy_quant": ("bwd", 179.48e6), "fwd_gemm": ("gemm", 64.09e6),
+              "dx_gemm": ("gemm", 52.94e6), "dw_gemm": ("gemm", 69.46e6)},
 }
 
 

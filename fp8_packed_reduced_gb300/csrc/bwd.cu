@@ -111,15 +111,6 @@ __device__ __forceinline__ void row_state(const BwdParams& p, const BwdUnit& b, 
   pos = __ldg(p.pos + t);
 }
 
-__device__ __forceinline__ void group_sync(int g) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(kGroupThreads) : "memory");
-}
-// The same barrier, placed after `dep` is computed: a value derived from
-// shared-memory reads pins those reads before the barrier in issue order.
-__device__ __forceinline__ void group_sync_after(int g, float dep) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(kGroupThreads), "f"(dep) : "memory");
-}
-
 // AND of `v` over the threads of consumer group g (all of them call it), so
 // that the group leaves its loop together.
 __device__ __forceinline__ bool group_all(int g, bool v) {
@@ -135,12 +126,6 @@ __device__ __forceinline__ bool group_all(int g, bool v) {
   return out != 0;
 }
 
-// Pass 2: the group's previous TMA store has finished reading its code
-// staging, which the group is about to overwrite.
-__device__ __forceinline__ void staging_free(int g, int gt) {
-  if (gt == 0) bulk_wait_read<0>();
-  group_sync(g);
-}
 
 // One kernel body for both passes.  QUANT = false: amax partials; true: codes.
 template <int DQK, bool QUANT>
@@ -154,6 +139,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[2 * kMaxStagesPerGroup];
+  // per group: every thread of the group is done with its current stage (and,
+  // in pass 2, has staged its codes); the group's thread 0 waits on it alone
+  __shared__ __align__(8) uint64_t done[2];
   __shared__ float red[32];
   __shared__ int abort_flag;
   const int g = threadIdx.x / kGroupThreads;    // consumer group
@@ -164,6 +152,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < 2 * SPG; ++s) mbar_init(&full[s], 1);
+    for (int gg = 0; gg < 2; ++gg) mbar_init(&done[gg], kGroupThreads);
     fence_mbar_init();
   }
   __syncthreads();
@@ -248,7 +237,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BwdUnit bn = bwd_decode(p, un);
       if (bn.part < 2) row_state(p, bn, bn.t0 + r, rstd_next, pos_next);
     }
-    if (!group_all(g, mbar_wait(&gfull[s], par, &abort_flag, st, kid))) break;
+    // (pass 2: thread 0 first lets the previous unit's codes leave the
+    // staging, which this unit overwrites after the barrier)
+    if (QUANT && gt == 0) bulk_wait_read<0>();
+    if (!group_all(g, mbar_wait(&gfull[s], par, &abort_flag, st, kid) && !abort_flag)) break;
     if (gt == 0) inflight &= ~(1u << s);
     const uint8_t* in0 = stages + s * kStage;
     int nbox;
@@ -267,7 +259,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       dot += __shfl_xor_sync(0xffffffffu, dot, 1);   // the row's other half
       const float mu = __fdiv_rn(dot, static_cast<float>(DQK));
       const f2 nmu = f2_make(-mu, -mu), rr = f2_make(rstd, rstd);
-      if (QUANT) staging_free(g, gt);
 #pragma unroll
       for (int gg = 0; gg < NG; ++gg) {
         const int c = 16 * gg + 8 * hf;
@@ -297,26 +288,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       nbox = DQK / 32;
-      if (QUANT) fence_async_smem();
-      // every value read from the stage has been used by now (see the v path)
-      group_sync_after(g, mx);   // the stage is read (and, in pass 2, the codes are staged)
-      if (gt == 0 && unit_at(k + SPG) >= 0) load_unit(unit_at(k + SPG), s, par ^ 1u);
     } else {
       uint4 x[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) x[q] = load8(in0, r, 16 * q + 8 * hf);
-      // The values are used before the group barrier below: a barrier does
-      // not wait for shared-memory reads still in flight, and the TMA refill
-      // it releases would race with them.
       if (QUANT) {
-        staging_free(g, gt);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const f2 v[4] = {f2_from_bf16x2(x[q].x), f2_from_bf16x2(x[q].y), f2_from_bf16x2(x[q].z),
                            f2_from_bf16x2(x[q].w)};
           emit8(v, kq, r, 16 * q + 8 * hf, out8);
         }
-        fence_async_smem();
       } else {
         // |bf16| orders as its 15 magnitude bits: max over packed halves
         uint32_t m2 = 0;
@@ -329,13 +311,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mx = fmax3(mx, bf16_lo(m2), bf16_hi(m2));
       }
-      group_sync_after(g, mx);   // the stage is read (and, in pass 2, the codes are staged)
-      if (gt == 0 && unit_at(k + SPG) >= 0) load_unit(unit_at(k + SPG), s, par ^ 1u);
       nbox = 4;
     }
-    if (QUANT && gt == 0) {
-      for (int j = 0; j < nbox; ++j) tma_store_2d(&m.dy8, out8 + j * kOutBox, b.col0 + 32 * j, b.t0);
-      bulk_commit();
+    // This thread is done with the stage: its reads are performed before the
+    // arrival (release), and in pass 2 its staged codes are made visible to
+    // the TMA store first.  Thread 0 alone waits for the whole group, then
+    // refills the stage and stores the codes.
+    if (QUANT) fence_async_smem();
+    mbar_arrive(&done[g]);
+    if (gt == 0 && mbar_wait(&done[g], k & 1, &abort_flag, st, kid)) {
+      if (unit_at(k + SPG) >= 0) load_unit(unit_at(k + SPG), s, par ^ 1u);
+      if (QUANT) {
+        for (int j = 0; j < nbox; ++j) tma_store_2d(&m.dy8, out8 + j * kOutBox, b.col0 + 32 * j, b.t0);
+        bulk_commit();
+      }
     }
   }
   if (gt == 0) {

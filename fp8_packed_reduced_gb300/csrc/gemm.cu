@@ -251,15 +251,23 @@ __device__ __forceinline__ void gemm_body(const Sched& sc, Epi& epi, const CUten
       epi.prepare(u);  // loads that do not depend on the accumulator
       if (!mbar_wait(&g.tfull[buf], (it >> 1) & 1, &g.abort_flag, st, kid)) break;
       tc_fence_after();
-      epi.process(u, tmem_base + static_cast<uint32_t>(buf * 256) + (static_cast<uint32_t>(qw * 32) << 16));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR)
-          mbar_arrive_cluster(tempty0 + 8u * static_cast<uint32_t>(buf));
-        else
-          mbar_arrive(&g.tempty[buf]);
-      }
+      // The epilogue calls `release` (once, with the whole warp) as soon as
+      // its last read of the accumulator has completed, so that the MMAs of
+      // a later unit may overwrite the buffer while it finishes.
+      bool released = false;
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster(tempty0 + 8u * static_cast<uint32_t>(buf));
+          else
+            mbar_arrive(&g.tempty[buf]);
+        }
+        released = true;
+      };
+      epi.process(u, tmem_base + static_cast<uint32_t>(buf * 256) + (static_cast<uint32_t>(qw * 32) << 16), release);
+      if (!released) release();
       epi.post(u);   // work after the accumulator buffer is released
     }
     epi.finish();
@@ -405,11 +413,13 @@ struct FwdEpi {
     return stage;
   }
 
-  __device__ void process(int u, uint32_t tacc) {
+  template <class Release>
+  __device__ void process(int u, uint32_t tacc, Release& release) {
     constexpr int HALF = DQK / 2;
     const int ty = sc.mtile(u) * kBM + qw * 32;
     for (int hh = sub; hh < nh; hh += nsub) {  // this warp's heads of the unit
       const int h = head0 + hh;
+      const bool last_head = hh + nsub >= nh;
       uint8_t* buf = acquire();
       if (kind < 2) {
         // pass 1: sum of squares of the raw accumulators (scaled once below)
@@ -441,6 +451,7 @@ struct FwdEpi {
           tmem_ld16(tacc + hh * DQK + g * 16, ra);
           tmem_ld16(tacc + hh * DQK + HALF + g * 16, rb);
           tmem_ld_wait();
+          if (last_head && g == HALF / 16 - 1) release();
           uint32_t lo[8], hi[8];
 #pragma unroll
           for (int w = 0; w < 8; ++w) {
@@ -468,6 +479,7 @@ struct FwdEpi {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld16(tacc + hh * 128 + hf * 64 + 16 * c, raw + 16 * c);
           tmem_ld_wait();
+          if (last_head && hf == 1) release();
           const f2 sc = f2_make(sxw, sxw);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -603,7 +615,8 @@ struct DxEpi {
     }
   }
   __device__ void post(int) {}
-  __device__ void process(int u, uint32_t tacc) {
+  template <class Release>
+  __device__ void process(int u, uint32_t tacc, Release& release) {
     const int m = sc.mtile(u), j = u % p.n_tiles;
     const int ty = m * kBM + qw * 32;
     const int share = p.bn / nsub;   // this warp's columns: [sub * share, (sub + 1) * share)
@@ -618,6 +631,7 @@ struct DxEpi {
       tmem_ld16(tacc + c0, raw);
       tmem_ld16(tacc + c0 + 16, raw + 16);
       tmem_ld_wait();
+      if (32 * (c + 1) >= share) release();   // the last chunk's accumulator is read
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]) * scl;
@@ -735,7 +749,8 @@ struct DwEpi {
   }
   // float4 index of columns [c, c + 4) of row `row` inside a partial tile
   __device__ static int quad(int c, int row) { return (c >> 2) * kBM + row; }
-  __device__ void process(int u, uint32_t tacc) {
+  template <class Release>
+  __device__ void process(int u, uint32_t tacc, Release& release) {
     last = false;
     // the odd CTA of the last pair may lie past the rows
     if (sc.mtile(u) >= p.m_tiles) return;
@@ -752,6 +767,7 @@ struct DwEpi {
         dst[quad(c0 + 4 * i, row)] = make_float4(__uint_as_float(raw[4 * i]), __uint_as_float(raw[4 * i + 1]),
                                                  __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3]));
     }
+    release();   // the accumulator is read
     __threadfence();   // this lane's stores are visible device-wide before the count
     __syncwarp();
     int old = 0;

@@ -468,8 +468,15 @@ def run_mlp(args, dev, world):
 
 def run_e2e(st: Step, args, dev, world):
     """Same metric through the public API with pinned host buffers: every step
-    copies the step's inputs host->device and its results device->host."""
+    copies the step's inputs host->device and its results device->host.  As an
+    input pipeline would, the copies overlap the neighbouring steps' compute:
+    two sets of device buffers, the uploads on one stream, the step on a
+    second, the downloads on a third, ordered by events (step i's uploads wait
+    until step i-2 has finished with that buffer set, its downloads until step
+    i has computed)."""
     qk = st.qk
+    sets = [st, Step(st.s, dev)]
+    torch.cuda.synchronize()   # the second set is built on the default stream
     h = dict(x=st.x.cpu().pin_memory(), dq=st.dq.cpu().pin_memory(), dk=st.dk.cpu().pin_memory(),
              dv=st.dv.cpu().pin_memory(), pos=st.pos.cpu().pin_memory())
     res = dict(q=torch.empty_like(st.fwd_out["q"], device="cpu").pin_memory(),
@@ -479,35 +486,55 @@ def run_e2e(st: Step, args, dev, world):
                dW=torch.empty_like(st.bwd_out["dW"], device="cpu").pin_memory())
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = sum(t.numel() * t.element_size() for t in res.values())
+    s_in, s_c, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "comp", "out")}
 
-    def one():
-        st.x.copy_(h["x"], non_blocking=True)
-        st.pos.copy_(h["pos"], non_blocking=True)
-        st.dq.copy_(h["dq"], non_blocking=True)
-        st.dk.copy_(h["dk"], non_blocking=True)
-        st.dv.copy_(h["dv"], non_blocking=True)
-        st.step()
-        res["q"].copy_(st.fwd_out["q"], non_blocking=True)
-        res["k"].copy_(st.fwd_out["k"], non_blocking=True)
-        res["v"].copy_(st.fwd_out["v"], non_blocking=True)
-        res["dx"].copy_(st.bwd_out["dx"], non_blocking=True)
-        res["dW"].copy_(st.bwd_out["dW"], non_blocking=True)
+    def one(i):
+        b, j = sets[i % 2], i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["comp"][j])      # step i-2 is done with these inputs
+            b.x.copy_(h["x"], non_blocking=True)
+            b.pos.copy_(h["pos"], non_blocking=True)
+            b.dq.copy_(h["dq"], non_blocking=True)
+            b.dk.copy_(h["dk"], non_blocking=True)
+            b.dv.copy_(h["dv"], non_blocking=True)
+            ev["in"][j].record(s_in)
+        with torch.cuda.stream(s_c):
+            s_c.wait_event(ev["in"][j])
+            if i >= 2:
+                s_c.wait_event(ev["out"][j])        # step i-2's results have been read out
+            b.step()
+            ev["comp"][j].record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][j])
+            res["q"].copy_(b.fwd_out["q"], non_blocking=True)
+            res["k"].copy_(b.fwd_out["k"], non_blocking=True)
+            res["v"].copy_(b.fwd_out["v"], non_blocking=True)
+            res["dx"].copy_(b.bwd_out["dx"], non_blocking=True)
+            res["dW"].copy_(b.bwd_out["dW"], non_blocking=True)
+            ev["out"][j].record(s_out)
 
     steps = max(3, min(args.steps, 50))
-    for _ in range(3):
-        one()
+    for i in range(4):
+        one(i)
+    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
+    a.record(s_in)
+    for i in range(steps):
+        one(i)
+    b.record(s_out)
     torch.cuda.synchronize()
+    for b_ in sets:
+        code, where = qk.poll_device_status(b_.ws)
+        if code != 0:
+            raise RuntimeError(f"device status {qk.STATUS.get(code)} from kernel {where}")
     ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
     return {"value": round(job_tokens_per_s(st.s.T, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
-            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "uploads, compute and downloads of neighbouring steps on three streams"}
 
 
 # ----------------------------------------------------------------------------

@@ -82,6 +82,10 @@ def lib() -> ctypes.CDLL:
             "qkvp_oproj_forward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 7 + [ctypes.c_size_t, _P]),
             "qkvp_oproj_backward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 10 + [ctypes.c_size_t, _P]),
             "qkvp_mlp_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 3),
+            "qkvp_activation_workspace_bytes": (ctypes.c_size_t, []),
+            "qkvp_quantize_activation": (ctypes.c_int, [_P, ctypes.c_int64, _P, _P, _P, ctypes.c_size_t, _P]),
+            "qkvp_forward_quantized": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_float, _P, ctypes.c_int]
+                                       + [_P] * 10 + [ctypes.c_size_t, _P]),
             "qkvp_mlp_forward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 12 + [ctypes.c_size_t, _P]),
             "qkvp_mlp_backward": (ctypes.c_int, [ctypes.c_int] * 3 + [_P] * 18 + [ctypes.c_size_t, _P]),
         }
@@ -318,6 +322,56 @@ def forward(x, pos, W8, w_scale, H, rope_table, d_qk=96, d_v=128, eps=1e-6, ws=N
                             _stream(dev))
     _check(rc, "qkvp_forward")
     saved = Saved(q=o["q"], k=o["k"], rstd=o["rstd"], x8=o["x8"], x_scale=o["x_scale"], pos=pos)
+    return o["q"], o["k"], o["v"], saved
+
+
+def quantize_activation(x, ws, out=None):
+    """Per-tensor E4M3 codes of a bf16 tensor (numel a multiple of 16).
+    ``ws``: a zero-initialised workspace (new_workspace, or any workspace of
+    this library).  Returns (codes uint8 shaped like x, scale [1] float32)."""
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(ws, "ws", torch.uint8)
+    if out is None:
+        out = (torch.empty(x.shape, dtype=torch.uint8, device=x.device),
+               torch.empty((1,), dtype=torch.float32, device=x.device))
+    x8, scale = out
+    _need_cuda(x8, "x8", torch.uint8, tuple(x.shape))
+    _need_cuda(scale, "scale", torch.float32, (1,))
+    _check(lib().qkvp_quantize_activation(_ptr(x), x.numel(), _ptr(x8), _ptr(scale), _ptr(ws), ws.numel(),
+                                          _stream(x.device)), "qkvp_quantize_activation")
+    return x8, scale
+
+
+def forward_quantized(x8, x_scale, pos, W8, w_scale, H, rope_table, d_qk=96, d_v=128, eps=1e-6, ws=None, out=None):
+    """The forward's GEMM and fused epilogue from x8 [T, D] and x_scale
+    (quantize_activation of x).  Returns (q, k, v, Saved) like forward()."""
+    T, D = x8.shape
+    shape = Shape(T, D, H, d_qk, d_v)
+    _need_cuda(x8, "x8", torch.uint8)
+    _need_cuda(x_scale, "x_scale", torch.float32, (1,))
+    _need_cuda(pos, "pos", torch.int32, (T,))
+    _need_cuda(W8, "W8", torch.uint8, (shape.N, D))
+    _need_cuda(w_scale, "w_scale", torch.float32, (1,))
+    _need_cuda(rope_table, "rope_table", torch.float32)
+    if rope_table.dim() != 3 or rope_table.shape[0] != d_qk // 4 or rope_table.shape[2] != 4:
+        raise ValueError("rope_table must be build_rope_table(max_pos, d_qk)")
+    dev = x8.device
+    if ws is None:
+        ws = new_workspace(shape, dev)
+    if out is None:
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        out = dict(q=torch.empty((H, T, d_qk), **bf), k=torch.empty((H, T, d_qk), **bf),
+                   v=torch.empty((H, T, d_v), **bf), rstd=torch.empty((2, H, T), dtype=torch.float32, device=dev))
+    o = out
+    for name, dt, shp in (("q", torch.bfloat16, (H, T, d_qk)), ("k", torch.bfloat16, (H, T, d_qk)),
+                          ("v", torch.bfloat16, (H, T, d_v)), ("rstd", torch.float32, (2, H, T))):
+        _need_cuda(o[name], name, dt, shp)
+    d = shape.dims()
+    _check(lib().qkvp_forward_quantized(ctypes.byref(d), eps, _ptr(rope_table), rope_table.shape[1], _ptr(x8),
+                                        _ptr(x_scale), _ptr(pos), _ptr(W8), _ptr(w_scale), _ptr(o["q"]),
+                                        _ptr(o["k"]), _ptr(o["v"]), _ptr(o["rstd"]), _ptr(ws), ws.numel(),
+                                        _stream(dev)), "qkvp_forward_quantized")
+    saved = Saved(q=o["q"], k=o["k"], rstd=o["rstd"], x8=x8, x_scale=x_scale, pos=pos)
     return o["q"], o["k"], o["v"], saved
 
 

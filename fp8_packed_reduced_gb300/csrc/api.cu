@@ -372,29 +372,15 @@ int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v, const uint16_t* c
   return QKVP_OK;
 }
 
-int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int max_pos, const uint16_t* x,
-                 const int32_t* pos, const uint8_t* W8, const float* w_scale, uint16_t* q, uint16_t* k,
-                 uint16_t* v, float* rstd, uint8_t* x8, float* x_scale, void* ws, size_t ws_bytes, void* stream) {
-  int rc = check_dims(dims);
-  if (rc != QKVP_OK) return rc;
-  if (!rope_table || !x || !pos || !W8 || !w_scale || !q || !k || !v || !rstd || !x8 || !x_scale || !ws)
-    return QKVP_ERR_INVALID_ARGUMENT;
-  if (max_pos < 1 || !(eps >= 0.f) || !(eps < 1.f)) return QKVP_ERR_INVALID_ARGUMENT;
-  const void* ptrs[] = {rope_table, x, pos, W8, w_scale, q, k, v, rstd, x8, x_scale, ws};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
-  if (ws_bytes < ws_bytes_for(dims)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
-  const int sms = sm_count();
-  if (sms <= 0) return QKVP_ERR_CUDA;
-
+namespace {
+// The packed GEMM with its fused epilogue, from x8 and its scale (arguments
+// already validated).
+int forward_gemm(const qkvp_dims* dims, float eps, const float* rope_table, int max_pos, const uint8_t* x8,
+                 const float* x_scale, const int32_t* pos, const uint8_t* W8, const float* w_scale, uint16_t* q,
+                 uint16_t* k, uint16_t* v, float* rstd, void* ws, int sms, cudaStream_t s) {
   const int T = dims->T, D = dims->D, H = dims->H, dqk = dims->d_qk, dv = dims->d_v;
   const int N = H * (2 * dqk + dv);
   const int tiles = (T + 127) / 128;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  float* xparts = reinterpret_cast<float*>(wsb + kStatusBytes);
-  const DevStatus st = dev_status(ws);
-
   // Tiles of the packed GEMM cover whole heads: q/k tiles of hq heads (the
   // last one may hold fewer), v tiles of 2 heads.  Each stage loads B as one
   // box of the full tile height, hq*d_qk rows (q/k) or 2*d_v rows (v), or
@@ -410,10 +396,6 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   ok = ok && map3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return QKVP_ERR_CUDA;
-
-  rc = quantize_activation(x, static_cast<int64_t>(T) * D, x8, xparts, x_scale, ws, s);
-  if (rc != QKVP_OK) return rc;
-
   FwdParams p;
   p.T = T;
   p.H = H;
@@ -433,9 +415,63 @@ int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.max_pos = max_pos;
   p.pos = pos;
   p.rstd = rstd;
-  QKVP_TRY_CUDA(launch_fwd_gemm(tm_x8, tm_w, tm_wv, tm_q, tm_k, tm_v, p, sms, st, s));
+  QKVP_TRY_CUDA(launch_fwd_gemm(tm_x8, tm_w, tm_wv, tm_q, tm_k, tm_v, p, sms, dev_status(ws), s));
   mark(s);
   return QKVP_OK;
+}
+}  // namespace
+
+int qkvp_forward(const qkvp_dims* dims, float eps, const float* rope_table, int max_pos, const uint16_t* x,
+                 const int32_t* pos, const uint8_t* W8, const float* w_scale, uint16_t* q, uint16_t* k,
+                 uint16_t* v, float* rstd, uint8_t* x8, float* x_scale, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != QKVP_OK) return rc;
+  if (!rope_table || !x || !pos || !W8 || !w_scale || !q || !k || !v || !rstd || !x8 || !x_scale || !ws)
+    return QKVP_ERR_INVALID_ARGUMENT;
+  if (max_pos < 1 || !(eps >= 0.f) || !(eps < 1.f)) return QKVP_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {rope_table, x, pos, W8, w_scale, q, k, v, rstd, x8, x_scale, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < ws_bytes_for(dims)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return QKVP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* xparts = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  rc = quantize_activation(x, static_cast<int64_t>(dims->T) * dims->D, x8, xparts, x_scale, ws, s);
+  if (rc != QKVP_OK) return rc;
+  return forward_gemm(dims, eps, rope_table, max_pos, x8, x_scale, pos, W8, w_scale, q, k, v, rstd, ws, sms, s);
+}
+
+size_t qkvp_activation_workspace_bytes(void) { return kStatusBytes + kPartsBytes; }
+
+int qkvp_quantize_activation(const uint16_t* x, int64_t n, uint8_t* x8, float* x_scale, void* ws, size_t ws_bytes,
+                             void* stream) {
+  if (!x || !x8 || !x_scale || !ws || n < 1) return QKVP_ERR_INVALID_ARGUMENT;
+  if (n % 16 != 0 || n > (int64_t(1) << 40)) return QKVP_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(x8) || !aligned16(x_scale) || !aligned16(ws)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < qkvp_activation_workspace_bytes()) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  float* parts = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  return quantize_activation(x, n, x8, parts, x_scale, ws, static_cast<cudaStream_t>(stream));
+}
+
+int qkvp_forward_quantized(const qkvp_dims* dims, float eps, const float* rope_table, int max_pos, const uint8_t* x8,
+                           const float* x_scale, const int32_t* pos, const uint8_t* W8, const float* w_scale,
+                           uint16_t* q, uint16_t* k, uint16_t* v, float* rstd, void* ws, size_t ws_bytes,
+                           void* stream) {
+  int rc = check_dims(dims);
+  if (rc != QKVP_OK) return rc;
+  if (!rope_table || !x8 || !x_scale || !pos || !W8 || !w_scale || !q || !k || !v || !rstd || !ws)
+    return QKVP_ERR_INVALID_ARGUMENT;
+  if (max_pos < 1 || !(eps >= 0.f) || !(eps < 1.f)) return QKVP_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {rope_table, x8, x_scale, pos, W8, w_scale, q, k, v, rstd, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QKVP_ERR_MISALIGNED;
+  if (ws_bytes < ws_bytes_for(dims)) return QKVP_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return QKVP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  mark(s);
+  return forward_gemm(dims, eps, rope_table, max_pos, x8, x_scale, pos, W8, w_scale, q, k, v, rstd, ws, sms, s);
 }
 
 int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, const uint16_t* dq,

@@ -165,6 +165,33 @@ int qkvp_forward(const qkvp_dims* dims, float eps,
                  uint8_t* x8, float* x_scale,
                  void* ws, size_t ws_bytes, void* stream);
 
+/* The two halves of qkvp_forward as separate calls, so that independent work
+ * (for example the bank refresh, on another stream) can run while x is
+ * quantised, before the GEMM that needs both.
+ *
+ * Per-tensor quantisation of any bf16 activation: scale s = amax/448 and
+ * codes E(v / s), in one launch (amax, a grid-wide barrier, codes).
+ *   x        in  n bf16 values (n a multiple of 16)
+ *   x8       out n codes          x_scale out [1] float32
+ *   ws       scratch of qkvp_activation_workspace_bytes() bytes, or the
+ *            workspace of a forward/backward (its start serves); zeroed
+ *            once with qkvp_workspace_init.  Calls sharing it must not
+ *            overlap on the GPU. */
+size_t qkvp_activation_workspace_bytes(void);
+int qkvp_quantize_activation(const uint16_t* x, int64_t n, uint8_t* x8, float* x_scale,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* The forward's packed GEMM and fused epilogue from x8 and x_scale already
+ * computed (by qkvp_quantize_activation on x [T, D]); the other arguments
+ * and results as in qkvp_forward.  qkvp_forward = qkvp_quantize_activation +
+ * qkvp_forward_quantized, with identical results. */
+int qkvp_forward_quantized(const qkvp_dims* dims, float eps,
+                           const float* rope_table, int max_pos,
+                           const uint8_t* x8, const float* x_scale, const int32_t* pos,
+                           const uint8_t* W8, const float* w_scale,
+                           uint16_t* q, uint16_t* k, uint16_t* v, float* rstd,
+                           void* ws, size_t ws_bytes, void* stream);
+
 /* Backward of the forward above ("Track 1 ... packed FP8 attention", sections
  * "Changes" and "Speed": FP8 backward using the cached transposed bank).
  * y is rebuilt from the saved outputs, y = RoPE^T(q), and

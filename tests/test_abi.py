@@ -170,6 +170,25 @@ def test_mlp_validation_codes(qk):
     assert bwd(128, 768, 3072, *bargs, p, 64, None) == qk.ERR_WORKSPACE_TOO_SMALL
 
 
+def test_split_forward_validation_codes(qk):
+    lib = qk.lib()
+    p = ctypes.c_void_p(4096)
+    n = lib.qkvp_activation_workspace_bytes()
+    assert n > 0
+    qa = lib.qkvp_quantize_activation
+    assert qa(None, 64, p, p, p, n, None) == qk.ERR_INVALID_ARGUMENT
+    assert qa(p, 0, p, p, p, n, None) == qk.ERR_INVALID_ARGUMENT
+    assert qa(p, 40, p, p, p, n, None) == qk.ERR_UNSUPPORTED
+    assert qa(p, 64, ctypes.c_void_p(4097), p, p, n, None) == qk.ERR_MISALIGNED
+    assert qa(p, 64, p, p, p, 16, None) == qk.ERR_WORKSPACE_TOO_SMALL
+    fq = lib.qkvp_forward_quantized
+    dims = qk.Dims(128, 768, 6, 96, 128)
+    assert fq(ctypes.byref(dims), 1e-6, p, 128, *([p] * 9), None, 1 << 40, None) == qk.ERR_INVALID_ARGUMENT
+    assert fq(ctypes.byref(dims), 1e-6, p, 128, *([p] * 10), 64, None) == qk.ERR_WORKSPACE_TOO_SMALL
+    bad = qk.Dims(128, 768, 6, 80, 128)
+    assert fq(ctypes.byref(bad), 1e-6, p, 128, *([p] * 10), 1 << 40, None) == qk.ERR_UNSUPPORTED
+
+
 def test_product_path_refuses_without_library(tmp_path, monkeypatch):
     import fp8_packed_reduced_gb300 as pkg
     monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -123,6 +123,38 @@ def test_forward_matches_oracle(qk, s):
     _check_forward(qk, s)
 
 
+def test_split_forward_equals_forward(qk):
+    """quantize_activation + forward_quantized give forward()'s results bit for
+    bit; the codes are the oracle's."""
+    s = synth.Shape(T=300, D=768, H=6, seq_len=256)
+    r = _run_forward(qk, s)
+    inp = r["inp"]
+    x8, sx = qk.quantize_activation(inp["x"].to(DEV), r["ws"])
+    q, k, v, saved = qk.forward_quantized(x8, sx, inp["pos"].to(DEV), r["W8"], r["w_scale"], s.H, r["table"],
+                                          ws=r["ws"])
+    torch.cuda.synchronize()
+    assert qk.poll_device_status(r["ws"]) == (qk.OK, 0)
+    assert torch.equal(x8, r["x8"]) and sx.item() == r["saved"].x_scale.item()
+    for name, t in (("q", q), ("k", k), ("v", v), ("rstd", saved.rstd)):
+        assert torch.equal(t, r[name] if name != "rstd" else r["saved"].rstd), name
+    codes, scale, _ = oracle.quantize(f32(inp["x"]))
+    np.testing.assert_array_equal(x8.cpu().numpy(), codes)
+    assert sx.item() == float(scale)
+
+
+@pytest.mark.parametrize("n", [16, 48, 4096 + 16, 3 * 2 ** 20])
+def test_quantize_activation_any_size(qk, n):
+    g = torch.Generator().manual_seed(n)
+    x = (torch.randn(n, generator=g) * 3).to(torch.bfloat16)
+    ws = qk.new_workspace(qk.Shape(128, 768, 6), DEV)
+    x8, sx = qk.quantize_activation(x.to(DEV), ws)
+    torch.cuda.synchronize()
+    assert qk.poll_device_status(ws) == (qk.OK, 0)
+    codes, scale, _ = oracle.quantize(f32(x))
+    np.testing.assert_array_equal(x8.cpu().numpy(), codes)
+    assert sx.item() == float(scale)
+
+
 def test_forward_deterministic(qk):
     s = synth.Shape(T=520, D=768, H=6, seq_len=512)
     a, b = _run_forward(qk, s), _run_forward(qk, s)

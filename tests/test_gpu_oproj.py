@@ -109,3 +109,18 @@ def test_oproj_full_size_sampled(qk):
     assert_close(r["da"][rows], da_ref, "da (sampled rows)")
     _, dWo_ref = oracle.oproj_grad_gemms(g8, s_g, oW8, os_o, a8, s_a)
     assert_close(r["dWo"], dWo_ref, "dWo")
+
+
+@pytest.mark.parametrize("R,C", [(768, 768), (3072, 768), (640, 1024)])
+def test_weight_refresh_several_matrices(qk, R, C):
+    """Three matrices in one call: each with its own scale, codes bit-exact in
+    both layouts, and the transposed layout a byte-for-byte transpose."""
+    g = torch.Generator().manual_seed(R + C)
+    mats = [((torch.randn(R, C, generator=g) * (0.5 + i)) * C ** -0.5).to(torch.bfloat16) for i in range(3)]
+    W8, W8T, s = qk.quantize_weight([m.to(DEV) for m in mats])
+    torch.cuda.synchronize()
+    for i, m in enumerate(mats):
+        o8, o8T, os_ = oracle.quantize_weight(f32(m))
+        np.testing.assert_array_equal(W8[i].cpu().numpy(), o8)
+        np.testing.assert_array_equal(W8T[i].cpu().numpy(), o8T)
+        assert s[i].item() == float(os_)

@@ -176,7 +176,15 @@ int qkvp_forward(const qkvp_dims* dims, float eps,
  *   ws       scratch of qkvp_activation_workspace_bytes() bytes, or the
  *            workspace of a forward/backward (its start serves); zeroed
  *            once with qkvp_workspace_init.  Calls sharing it must not
- *            overlap on the GPU. */
+ *            overlap on the GPU.
+ * The launch is persistent and its blocks meet at a grid-wide barrier, so all
+ * of them must be resident at once: it may share the GPU with small kernels
+ * of other streams, but two of these quantisations (this call, or the one
+ * inside qkvp_forward / qkvp_oproj_* / qkvp_mlp_*) running concurrently on
+ * different streams, or a long persistent kernel holding the SMs, can keep
+ * blocks out until the wait limit (qkvp_set_wait_timeout_ns) expires; the
+ * call then reports QKVP_ERR_TIMEOUT through the status word instead of
+ * hanging.  Run such calls on one stream. */
 size_t qkvp_activation_workspace_bytes(void);
 int qkvp_quantize_activation(const uint16_t* x, int64_t n, uint8_t* x8, float* x_scale,
                              void* ws, size_t ws_bytes, void* stream);

@@ -70,9 +70,9 @@ def algorithmic_work(s: synth.Shape):
 KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu"}
 TRAFFIC = {
     "T": 24576,
-    "sources_sha256": {"bwd": "b3d41929d5febd1d9aa415f5d94aacbf89ecc8b6e494d96761e6af9b37a04e94", "gemm": "d6d7da1af52f2674366ae814ad5dbe89eb640ab0c99ccf6ee711b0ddffea7007"},
-    "bytes": {"dy_amax": ("bwd", 159.09e6), "dy_quant": ("bwd", 179.48e6), "fwd_gemm": ("gemm", 64.09e6),
-              "dx_gemm": ("gemm", 52.94e6), "dw_gemm": ("gemm", 69.46e6)},
+    "sources_sha256": {"bwd": "ac53343ef519ecf6996f223a2157156a15e5bf1b7eda7b8f0b11d18c6364000c", "gemm": "423682d3115563f0cc8123a7b829f2c52d0e2c3b785c3e56cf0cf99bd786341f"},
+    "bytes": {"dy_amax": ("bwd", 159.27e6), "dy_quant": ("bwd", 179.81e6), "fwd_gemm": ("gemm", 64.24e6),
+              "dx_gemm": ("gemm", 52.43e6), "dw_gemm": ("gemm", 69.11e6)},
 }
 
 

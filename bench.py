@@ -276,16 +276,25 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     assert all(e.cuda_event for ev in events for e in ev)
     # The K timed steps are captured once into one CUDA graph (as a training
-    # loop would run them), so host launch overhead stays out of the timing;
-    # the library records each step's kernel-boundary events inside the graph.
+    # loop would run them), so host launch overhead stays out of the timing.
+    # A second graph of the same K steps has the library record kernel-boundary
+    # events between its launches: replayed after the timed region, it gives
+    # the per-kernel breakdown.  (Event nodes between kernels break the
+    # back-to-back launch of dependent kernels, about 3 us each, so the timed
+    # graph has none.)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
+        for i in range(args.steps):
+            st.step()
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev):
         for i in range(args.steps):
             qk.set_timing_events(events[i])
             st.step()
         qk.set_timing_events([])
     torch.cuda.synchronize()
-    graph.replay()                  # one untimed replay: the graph's first launch uploads it
+    graph.replay()                  # one untimed replay each: a graph's first launch uploads it
+    graph_ev.replay()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
     sampler = ClockSampler(dev.index)
@@ -306,6 +315,8 @@ def run_ours(args, rank, world):
     sampler.mark("t1")
     clocks = sampler.stop()
     ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, world, dev)
+    graph_ev.replay()                # the per-kernel breakdown, after the timed region
+    torch.cuda.synchronize()
     code, where = qk.poll_device_status(st.ws)
     if code != 0:
         raise RuntimeError(f"device status {qk.STATUS.get(code)} from kernel {where}")
@@ -342,6 +353,8 @@ def run_ours(args, rank, world):
         "roofline": roofline, "kernels": kern,
         "gpu_launches": len(KERNELS) * args.steps,
         "launch": "the K timed steps replayed as one captured CUDA graph",
+        "kernel_timing": "per-kernel means from a second replay of the same K steps with kernel-boundary events "
+                         "(each event node adds about 3 us to the span it ends)",
         "clocks": clocks, "e2e": e2e,
     }
     if not args.no_next_rows:
@@ -352,10 +365,10 @@ def run_ours(args, rank, world):
 
 
 def time_in_graph(step, n_events, steps, warmup, dev, world, ws_list):
-    """Run `step` warmup times, capture `steps` calls in one CUDA graph with
-    the library's kernel-boundary events (n_events per call) and replay it
-    once untimed and once timed.  Returns (ms per step, max over ranks; list
-    of per-call event lists)."""
+    """Run `step` warmup times, capture `steps` calls in one CUDA graph (timed)
+    and again with the library's kernel-boundary events (n_events per call;
+    replayed after the timed region for the per-kernel breakdown).  Returns
+    (ms per step, max over ranks; list of per-call event lists)."""
     import fp8_packed_reduced_gb300 as qk
     for _ in range(max(3, warmup)):
         step()
@@ -369,11 +382,16 @@ def time_in_graph(step, n_events, steps, warmup, dev, world, ws_list):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for i in range(steps):
+            step()
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev):
+        for i in range(steps):
             qk.set_timing_events(events[i])
             step()
         qk.set_timing_events([])
     torch.cuda.synchronize()
     graph.replay()
+    graph_ev.replay()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -381,6 +399,8 @@ def time_in_graph(step, n_events, steps, warmup, dev, world, ws_list):
     t1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1) / steps, world, dev)
+    graph_ev.replay()
+    torch.cuda.synchronize()
     for ws in ws_list:
         code, where = qk.poll_device_status(ws)
         if code != 0:

@@ -188,12 +188,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // The group's k-th unit (-1 past the end): the q, k and v parts of one
   // (token tile, head) follow each other, the (tile, head) triples going
   // round-robin over the grid's groups.  The k part reuses the q part's RoPE
-  // factors (same tokens, same positions).
+  // factors (same tokens, same positions).  Pass 2 walks the triples in the
+  // opposite order, so that it starts on the inputs pass 1 read last, which
+  // are still in L2.
   const int g0 = blockIdx.x + g * gridDim.x;
   const int ntriples = p.num_units / 3;
   auto unit_at = [&](int k) -> int {
     const int tr = g0 + (k / 3) * ustep;
-    return tr < ntriples ? 3 * tr + k % 3 : -1;
+    if (tr >= ntriples) return -1;
+    return 3 * (QUANT ? ntriples - 1 - tr : tr) + k % 3;
   };
   if (gt == 0)
     for (int k = 0; k < SPG; ++k)

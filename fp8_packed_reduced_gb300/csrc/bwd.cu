@@ -171,16 +171,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // Input loads of unit u into stage s (thread gt == 0 only).  `inflight`
   // and `inpar` record the stages whose loads have not been waited for.
   uint32_t inflight = 0, inpar = 0;
+  const uint64_t stream = l2_policy_evict_first();
   auto load_unit = [&](int u, int s, uint32_t par) {
     const BwdUnit b = bwd_decode(p, u);
     uint8_t* in0 = stages + s * kStage;
     const int nbox = (b.part < 2 ? DQK : p.d_v) / 32;
     mbar_arrive_expect_tx(&gfull[s], static_cast<uint32_t>((b.part < 2 ? 2 : 1) * nbox * kInBox));
     const CUtensorMap* gm = b.part == 0 ? &m.dq : b.part == 1 ? &m.dk : &m.dv;
-    for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + j * kInBox, gm, &gfull[s], 32 * j, b.t0, b.h);
-    if (b.part < 2) {
-      const CUtensorMap* om = b.part == 0 ? &m.q : &m.k;
-      for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + (nbox + j) * kInBox, om, &gfull[s], 32 * j, b.t0, b.h);
+    const CUtensorMap* om = b.part == 0 ? &m.q : &m.k;
+    if (QUANT) {
+      for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + j * kInBox, gm, &gfull[s], 32 * j, b.t0, b.h);
+      if (b.part < 2)
+        for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + (nbox + j) * kInBox, om, &gfull[s], 32 * j, b.t0, b.h);
+    } else {
+      for (int j = 0; j < nbox; ++j) tma_load_3d_hint(in0 + j * kInBox, gm, &gfull[s], 32 * j, b.t0, b.h, stream);
+      if (b.part < 2)
+        for (int j = 0; j < nbox; ++j)
+          tma_load_3d_hint(in0 + (nbox + j) * kInBox, om, &gfull[s], 32 * j, b.t0, b.h, stream);
     }
     inflight |= 1u << s;
     inpar = (inpar & ~(1u << s)) | (par << s);
@@ -198,6 +205,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tr >= ntriples) return -1;
     return 3 * (QUANT ? ntriples - 1 - tr : tr) + k % 3;
   };
+  // Pass 1 streams its inputs through L2 marked evict-first (measured 5 us
+  // faster at the training shape than without a hint; marking its last
+  // rounds evict-last for pass 2 instead gained nothing); pass 2 loads
+  // without a hint (evict-first there was slower).
   if (gt == 0)
     for (int k = 0; k < SPG; ++k)
       if (unit_at(k) >= 0) load_unit(unit_at(k), k, 0);

@@ -234,16 +234,6 @@ __device__ __forceinline__ void grid_barrier(GridBar* bar, const DevStatus& st, 
 constexpr int kFusedThreads = 512;
 
 // 16-byte read-only load with an L2 eviction-priority policy (createpolicy).
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 __device__ __forceinline__ uint4 ldg_hint(const uint4* ptr, uint64_t pol) {
   uint4 v;
   asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"

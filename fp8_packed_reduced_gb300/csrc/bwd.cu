@@ -195,15 +195,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // The group's k-th unit (-1 past the end): the q, k and v parts of one
   // (token tile, head) follow each other, the (tile, head) triples going
   // round-robin over the grid's groups.  The k part reuses the q part's RoPE
-  // factors (same tokens, same positions).  Pass 2 walks the triples in the
-  // opposite order, so that it starts on the inputs pass 1 read last, which
-  // are still in L2.
+  // factors (same tokens, same positions).  Pass 1 walks the triples from
+  // the last token tile down, starting on the q and k the forward wrote last
+  // (still in L2); pass 2 walks them upwards, starting on the inputs pass 1
+  // read last.
   const int g0 = blockIdx.x + g * gridDim.x;
   const int ntriples = p.num_units / 3;
   auto unit_at = [&](int k) -> int {
     const int tr = g0 + (k / 3) * ustep;
     if (tr >= ntriples) return -1;
-    return 3 * (QUANT ? ntriples - 1 - tr : tr) + k % 3;
+    return 3 * (QUANT ? tr : ntriples - 1 - tr) + k % 3;
   };
   // Pass 1 streams its inputs through L2 marked evict-first (measured 5 us
   // faster at the training shape than without a hint; marking its last

@@ -183,6 +183,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + j * kInBox, gm, &gfull[s], 32 * j, b.t0, b.h);
       if (b.part < 2)
         for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + (nbox + j) * kInBox, om, &gfull[s], 32 * j, b.t0, b.h);
+    } else if (u / 3 < ustep) {   // pass 1's last round: kept in L2 for pass 2's first
+      for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + j * kInBox, gm, &gfull[s], 32 * j, b.t0, b.h);
+      if (b.part < 2)
+        for (int j = 0; j < nbox; ++j) tma_load_3d(in0 + (nbox + j) * kInBox, om, &gfull[s], 32 * j, b.t0, b.h);
     } else {
       for (int j = 0; j < nbox; ++j) tma_load_3d_hint(in0 + j * kInBox, gm, &gfull[s], 32 * j, b.t0, b.h, stream);
       if (b.part < 2)
@@ -207,9 +211,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     return 3 * (QUANT ? tr : ntriples - 1 - tr) + k % 3;
   };
   // Pass 1 streams its inputs through L2 marked evict-first (measured 5 us
-  // faster at the training shape than without a hint; marking its last
-  // rounds evict-last for pass 2 instead gained nothing); pass 2 loads
-  // without a hint (evict-first there was slower).
+  // faster at the training shape than without a hint), except its last round,
+  // which pass 2 reads first: that one is loaded without a hint (2 us off
+  // pass 2; two or three such rounds, or evict-last, gained no more).  Pass 2
+  // loads without a hint (evict-first there was slower).
   if (gt == 0)
     for (int k = 0; k < SPG; ++k)
       if (unit_at(k) >= 0) load_unit(unit_at(k), k, 0);

@@ -358,6 +358,7 @@ def run_ours(args, rank, world):
         "clocks": clocks, "e2e": e2e,
     }
     if not args.no_next_rows:
+        line["bank_refresh"] = run_bank_refresh(args, dev, load_peaks())
         line["next_rows"] = {"oproj": run_oproj(args, dev, world), "mlp": run_mlp(args, dev, world)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, args.cpu_sample)
@@ -500,6 +501,39 @@ def run_mlp(args, dev, world):
             "steps": steps, "kernels": kern, "gpu_launches": len(MLP_KERNELS) * steps}
 
 
+def run_bank_refresh(args, dev, peaks, L=12, repeats=20, warmup=4):
+    """The weight-bank workload: L layers of the packed bank [N, D] refreshed
+    from their bf16 sources in one call (amax, then both code layouts from one
+    read), alternating with a perturbed copy of the weights (an optimizer
+    update).  256 MB are written between refreshes to flush L2; each refresh is
+    timed alone with CUDA events on its stream."""
+    import fp8_packed_reduced_gb300 as qk
+    H, D, dqk, dv = args.H, args.D, args.dqk, 128
+    N = H * (2 * dqk + dv)
+    base = synth.bank_layers(L, H, D, dqk, dv, device=dev)
+    upd = synth.bank_layers(L, H, D, dqk, dv, perturb=1e-3, device=dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    out = (torch.empty((L, N, D), **u8), torch.empty((L, D, N), **u8), torch.empty((L,), dtype=torch.float32, device=dev))
+    flush = torch.empty(256 << 20, **u8)
+    spans = []
+    for i in range(warmup + repeats):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        qk.quantize_bank(base if i % 2 == 0 else upd, H, dqk, dv, out=out)
+        b.record()
+        if i >= warmup:
+            spans.append((a, b))
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in spans) / len(spans)
+    moved = L * (N * D * 2 + 2 * N * D)   # bf16 sources read once, both code layouts written
+    gbs = moved / (ms * 1e-3) / 1e9
+    return {"workload": f"bank refresh, {L} layers x [{N}, {D}] (alternating with a perturbed copy)",
+            "ms_per_refresh": round(ms, 5), "bytes": moved, "achieved": round(gbs, 1), "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm"], 4), "repeats": repeats, "l2": "256 MB written before each refresh",
+            "gpu_launches": 2 * repeats}
+
+
 def run_e2e(st: Step, args, dev, world):
     """Same metric through the public API with pinned host buffers: every step
     copies the step's inputs host->device and its results device->host.  As an
@@ -636,7 +670,7 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=1024, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
-                    help="skip the output-projection and MLP measurements")
+                    help="skip the bank-refresh, output-projection and MLP measurements")
     ap.add_argument("--cta-pairs", type=int, default=None,
                     help="GEMMs on 2-CTA clusters: bit 0 forward, bit 1 dX, bit 2 dW (default: the library's)")
     args = ap.parse_args()

@@ -3,6 +3,8 @@
 //   x amax        (per-tensor amax of the activations)
 //   x quantise    (codes of x, token-major)
 //   RoPE table, and the timeout self-test kernel.
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace qkvp {
@@ -51,10 +53,10 @@ cudaError_t launch_amax_bf16(const uint16_t* x, int64_t n, float* partials, int 
 // ---------------------------------------------------------------------------
 // Bank refresh.  Pass 1: amax of each layer's logical Q/K/V packs, read in
 // place (no concatenation).  Pass 2: every block re-reduces its layer's
-// partials, then converts a 128 x 128 tile of the bank and writes it to both
+// partials, then converts 128 x 128 tiles of the bank and writes each to both
 // W8 (row-major) and W8T (transposed) from the one read of that tile.  All
-// layers of a refresh go in one launch per pass; the second pass reads the
-// bank back from L2 for bank sizes that fit there.
+// layers of a refresh go in one launch per pass, each sized to one wave; the
+// second pass reads the bank back from L2 for bank sizes that fit there.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ const uint16_t* bank_row(const BankArgs& a, int l, int n) {
   if (n < a.Nq) return a.Wq[l] + static_cast<int64_t>(n) * a.D;
@@ -62,99 +64,151 @@ __device__ __forceinline__ const uint16_t* bank_row(const BankArgs& a, int l, in
   return a.Wv[l] + static_cast<int64_t>(n - 2 * a.Nq) * a.D;
 }
 
-// grid: (kBankAmaxBlocks, L), 1024 threads.
+// grid: (kBankAmaxBlocks, L), 1024 threads.  Block b of layer l takes a
+// contiguous band of rows; one warp per row, two rows in flight, the lanes
+// over the row's 16-byte chunks.
 __global__ void __launch_bounds__(1024) bank_amax_kernel(const __grid_constant__ BankArgs a, float* partials) {
   __shared__ float red[32];
   const int l = blockIdx.y;
-  const int row_chunks = a.D / 8;  // 16-byte chunks per row
-  const int64_t total = static_cast<int64_t>(a.N) * row_chunks;
+  const int cpr = a.D / 8;   // 16-byte chunks per row
+  const int band = (a.N + gridDim.x - 1) / gridDim.x;
+  const int r0 = blockIdx.x * band, r1 = min(a.N, r0 + band);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   float m = 0.f;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < total; i += 4 * stride) {  // four independent loads in flight
-    uint4 v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t e = i + j * stride;
-      v[j] = __ldg(reinterpret_cast<const uint4*>(bank_row(a, l, static_cast<int>(e / row_chunks))) +
-                   static_cast<int>(e % row_chunks));
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, absmax_bf16x8(v[j]));
+  int n = r0 + warp;
+  for (; n + nw < r1; n += 2 * nw) {
+    const uint4* ra = reinterpret_cast<const uint4*>(bank_row(a, l, n));
+    const uint4* rb = reinterpret_cast<const uint4*>(bank_row(a, l, n + nw));
+#pragma unroll 4
+    for (int c = lane; c < cpr; c += 32)
+      m = fmaxf(m, fmaxf(absmax_bf16x8(__ldg(ra + c)), absmax_bf16x8(__ldg(rb + c))));
   }
-  for (; i < total; i += stride) {
-    const int n = static_cast<int>(i / row_chunks), c = static_cast<int>(i % row_chunks);
-    m = fmaxf(m, absmax_bf16x8(__ldg(reinterpret_cast<const uint4*>(bank_row(a, l, n)) + c)));
+  if (n < r1) {
+    const uint4* ra = reinterpret_cast<const uint4*>(bank_row(a, l, n));
+#pragma unroll 4
+    for (int c = lane; c < cpr; c += 32) m = fmaxf(m, absmax_bf16x8(__ldg(ra + c)));
   }
   m = block_max(m, red);
   if (threadIdx.x == 0) partials[l * gridDim.x + blockIdx.x] = m;
 }
 
+// Transpose of a 4 x 4 byte block held as four row words: out[c] = bytes
+// (r0[c], r1[c], r2[c], r3[c]).
+__device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3, uint32_t (&out)[4]) {
+  const uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r0, r1, 0x7362);   // (r0c0 r1c0 r0c1 r1c1), (.. c2 .. c3)
+  const uint32_t t2 = __byte_perm(r2, r3, 0x5140), t3 = __byte_perm(r2, r3, 0x7362);
+  out[0] = __byte_perm(t0, t2, 0x5410);
+  out[1] = __byte_perm(t0, t2, 0x7632);
+  out[2] = __byte_perm(t1, t3, 0x5410);
+  out[3] = __byte_perm(t1, t3, 0x7632);
+}
+
 // grid: (ceil(N/128) * D/128, L); 256 threads; tile 128 rows x 128 columns.
+// Thread t converts rows 4 (t / 8) .. + 3, columns 16 (t % 8) .. + 15 of the
+// tile: one 16-byte code store per row into W8, and, transposed in registers
+// by 4 x 4 byte blocks, sixteen 4-byte column words into a shared tile [128
+// columns][32 words of 4 rows], whose word index is XORed with 4 * (column /
+// 16) % 32 so that a warp's stores hit 32 banks; the tile then leaves as
+// 16-byte chunks of W8T rows.
 __global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__ BankArgs a,
                                                          const float* partials) {
   __shared__ float red[32];
-  __shared__ __align__(16) uint8_t tr[128][128 + 16];  // [column][row] codes
+  __shared__ __align__(16) uint32_t tr[128][32];   // [tile column][row group, swizzled]
   const int l = blockIdx.y;
   const int tiles_d = a.D / 128;
-  const int n0 = (blockIdx.x / tiles_d) * 128, d0 = (blockIdx.x % tiles_d) * 128;
+  const int tiles = (a.N + 127) / 128 * tiles_d;
   const float amax = block_reduce_partials(partials + l * kBankAmaxBlocks, kBankAmaxBlocks, red);
   const float s = scale_from_amax(amax);
-  const Bracket k = make_bracket(s);
+  const Bracket2 k = make_bracket2(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) a.w_scale[l] = s;
 
-  const int r = threadIdx.x >> 1;          // tile row
-  const int ch = (threadIdx.x & 1) * 64;   // first of this thread's 64 columns
-  const int n = n0 + r;
+  const int rg = threadIdx.x >> 3, cg = threadIdx.x & 7;
   uint8_t* W8 = a.W8 + static_cast<int64_t>(l) * a.N * a.D;
   uint8_t* W8T = a.W8T + static_cast<int64_t>(l) * a.N * a.D;
-  if (n < a.N) {
-    const uint4* src = reinterpret_cast<const uint4*>(bank_row(a, l, n) + d0 + ch);
-    uint4 v[8];
+  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {   // the layer's tiles, round-robin
+  const int n0 = (tile / tiles_d) * 128, d0 = (tile % tiles_d) * 128;
+  if (tile != static_cast<int>(blockIdx.x)) __syncthreads();   // the previous tile has left `tr`
+  uint4 code[4];   // the four rows' 16 codes
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __ldg(src + j);
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      const uint32_t w[8] = {v[j].x, v[j].y, v[j].z, v[j].w, v[j + 1].x, v[j + 1].y, v[j + 1].z, v[j + 1].w};
-      uint32_t c[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        c[q] = quant4_fast(bf16_lo(w[2 * q]), bf16_hi(w[2 * q]), bf16_lo(w[2 * q + 1]), bf16_hi(w[2 * q + 1]), k);
-      *reinterpret_cast<uint4*>(W8 + static_cast<int64_t>(n) * a.D + d0 + ch + j * 8) =
-          make_uint4(c[0], c[1], c[2], c[3]);
-#pragma unroll
-      for (int b = 0; b < 16; ++b) tr[ch + j * 8 + b][r] = static_cast<uint8_t>(c[b >> 2] >> (8 * (b & 3)));
+  for (int i = 0; i < 4; ++i) {
+    const int n = n0 + 4 * rg + i;
+    if (n < a.N) {
+      const uint4* src = reinterpret_cast<const uint4*>(bank_row(a, l, n) + d0 + 16 * cg);
+      const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+      const f2 v0[4] = {f2_from_bf16x2(u0.x), f2_from_bf16x2(u0.y), f2_from_bf16x2(u0.z), f2_from_bf16x2(u0.w)};
+      const f2 v1[4] = {f2_from_bf16x2(u1.x), f2_from_bf16x2(u1.y), f2_from_bf16x2(u1.z), f2_from_bf16x2(u1.w)};
+      const uint2 c0 = quant8(v0, k), c1 = quant8(v1, k);
+      code[i] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+      *reinterpret_cast<uint4*>(W8 + static_cast<int64_t>(n) * a.D + d0 + 16 * cg) = code[i];
+    } else {
+      code[i] = make_uint4(0, 0, 0, 0);
     }
-  } else {
-#pragma unroll 1
-    for (int b = 0; b < 64; ++b) tr[ch + b][r] = 0;
+  }
+  // column 16 cg + 4 q + c holds the bytes of rows 4 rg .. 4 rg + 3
+  const int sw = (cg & 7) << 2;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+    const uint32_t* r = reinterpret_cast<const uint32_t*>(code);
+    transpose4x4(r[q], r[4 + q], r[8 + q], r[12 + q], w);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tr[16 * cg + 4 * q + c][rg ^ sw] = w[c];
   }
   __syncthreads();
-  // W8T rows d0..d0+127, columns n0..n0+127 (clipped at N); 16 bytes per step.
+  // W8T rows d0 .. d0 + 127, columns n0 .. n0 + 127 (N is a multiple of 64):
+  // chunk i (rows 16 i .. 16 i + 15 of the tile) of column col is the word
+  // group 4 i .. 4 i + 3, stored at 4 (i ^ (col / 16 % 8)).
   const int nvalid = min(128, a.N - n0);
-  for (int i = threadIdx.x; i < 128 * 8; i += 256) {
-    const int col = i >> 3, part = (i & 7) * 16;
-    if (part < nvalid) {
-      const uint4 val = *reinterpret_cast<const uint4*>(&tr[col][part]);
-      uint8_t* dst = W8T + static_cast<int64_t>(d0 + col) * a.N + n0 + part;
-      if (part + 16 <= nvalid) {
-        *reinterpret_cast<uint4*>(dst) = val;
-      } else {
-        const uint8_t* b = reinterpret_cast<const uint8_t*>(&val);
-        for (int q = 0; q < nvalid - part; ++q) dst[q] = b[q];
-      }
+  for (int e = threadIdx.x; e < 128 * 8; e += 256) {
+    const int col = e >> 3, i = e & 7;
+    if (16 * i < nvalid) {
+      const uint4 val = *reinterpret_cast<const uint4*>(&tr[col][4 * (i ^ ((col >> 4) & 7))]);
+      *reinterpret_cast<uint4*>(W8T + static_cast<int64_t>(d0 + col) * a.N + n0 + 16 * i) = val;
     }
+  }
   }
 }
 
+static int bank_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Up to 9 layers the amax grid fits the GPU in one wave of 1024-thread
+// blocks (two per SM); beyond that, blocks of 512 threads keep it to one.
 cudaError_t launch_bank_amax(const BankArgs& a, float* partials, cudaStream_t s) {
-  bank_amax_kernel<<<dim3(kBankAmaxBlocks, a.L), 1024, 0, s>>>(a, partials);
+  const int sms = bank_sms();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int threads = kBankAmaxBlocks * a.L <= 2 * sms ? 1024 : 512;
+  bank_amax_kernel<<<dim3(kBankAmaxBlocks, a.L), threads, 0, s>>>(a, partials);
   return cudaGetLastError();
 }
 
+// One block per tile while the tiles of all layers fit on the GPU at once;
+// beyond that each block takes several tiles of its layer (one wave).
 cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStream_t s) {
+  static int per_sm[64] = {};
+  const int sms = bank_sms();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int resident = dev < 64 ? per_sm[dev] : 0;
+  if (resident <= 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, bank_quant_kernel, 256, 0);
+    if (e != cudaSuccess) return e;
+    if (resident < 1) return cudaErrorInvalidConfiguration;
+    if (dev < 64) per_sm[dev] = resident;
+  }
   const int tiles = ((a.N + 127) / 128) * (a.D / 128);
-  bank_quant_kernel<<<dim3(tiles, a.L), 256, 0, s>>>(a, partials);
+  const int per_layer = std::max(1, std::min(tiles, resident * sms / a.L));
+  bank_quant_kernel<<<dim3(per_layer, a.L), 256, 0, s>>>(a, partials);
   return cudaGetLastError();
 }
 

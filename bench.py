@@ -351,7 +351,7 @@ def run_ours(args, rank, world):
                    "l2": "no flush; one step touches ~1.3 GB, 10x the 129 MB L2",
                    "gemm_cta_pairs": pairs},
         "roofline": roofline, "kernels": kern,
-        "gpu_launches": len(KERNELS) * args.steps,
+        "gpu_launches": (len(KERNELS) + 1) * args.steps,   # + the dW split reduction kernel
         "launch": "the K timed steps replayed as one captured CUDA graph",
         "kernel_timing": "per-kernel means from a second replay of the same K steps with kernel-boundary events "
                          "(each event node adds about 3 us to the span it ends)",
@@ -453,7 +453,7 @@ def run_oproj(args, dev, world):
     return {"workload": f"output projection over the V/O bank fwd+bwd, T={T}, D={D}, K=H*d_v={K}, "
                         "weight refresh per step",
             "value": round(job_tokens_per_s(T, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
-            "steps": steps, "kernels": kern, "gpu_launches": len(OPROJ_KERNELS) * steps}
+            "steps": steps, "kernels": kern, "gpu_launches": (len(OPROJ_KERNELS) + 1) * steps}
 
 
 MLP_KERNELS = ["w1_amax", "w1_quant", "w2_amax", "w2_quant", "x_quant", "fc_gemm", "h_quant", "proj_gemm",
@@ -498,7 +498,7 @@ def run_mlp(args, dev, world):
     kern = kernel_table(per, work, load_peaks())
     return {"workload": f"FP8 ReLU-squared MLP fwd+bwd, T={T}, D={D}, F={F_}, both weight refreshes per step",
             "value": round(job_tokens_per_s(T, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
-            "steps": steps, "kernels": kern, "gpu_launches": len(MLP_KERNELS) * steps}
+            "steps": steps, "kernels": kern, "gpu_launches": (len(MLP_KERNELS) + 2) * steps}
 
 
 def run_bank_refresh(args, dev, peaks, L=12, repeats=20, warmup=4):

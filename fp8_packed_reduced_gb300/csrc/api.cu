@@ -88,8 +88,7 @@ int check_dims(const qkvp_dims* d) {
   return QKVP_OK;
 }
 
-// Workspace: [status 256 B][x amax partials][dY amax partials][dW tile
-// counters][dW partials]
+// Workspace: [status 256 B][x amax partials][dY amax partials][dW partials]
 constexpr size_t kStatusBytes = 256;
 constexpr int kMaxParts = 4096;
 constexpr size_t kPartsBytes = kMaxParts * sizeof(float);
@@ -111,13 +110,7 @@ DwShape dw_shape(const qkvp_dims* d) { return dw_shape_rc(d->H * (2 * d->d_qk + 
 size_t dw_partial_bytes(const DwShape& s, int splits) {
   return static_cast<size_t>(splits) * s.m_tiles * s.n_tiles * s.bn * 128 * sizeof(float);
 }
-// one counter per (tile, dW epilogue warp), padded to 256 bytes
-size_t dw_counter_bytes(const DwShape& s) {
-  return (static_cast<size_t>(s.m_tiles) * s.n_tiles * kDwEpiWarps * sizeof(int) + 255) / 256 * 256;
-}
-size_t ws_bytes_for_shape(const DwShape& s) {
-  return kStatusBytes + 2 * kPartsBytes + dw_counter_bytes(s) + dw_partial_bytes(s, kMaxSplits);
-}
+size_t ws_bytes_for_shape(const DwShape& s) { return kStatusBytes + 2 * kPartsBytes + dw_partial_bytes(s, kMaxSplits); }
 size_t ws_bytes_for(const qkvp_dims* d) { return ws_bytes_for_shape(dw_shape(d)); }
 
 // Split count for the dW GEMM: the fewest splits whose units fill the
@@ -220,9 +213,9 @@ int gemm_nt(int T, int Nout, int K, const uint8_t* A8, const uint8_t* B8, const 
 
 // dW [R, C] bf16 = (G8 [T, R]^T . X8 [T, C]) * sg * sx, both operands read
 // MN-major (token-major codes as stored), split over the tokens; partials and
-// per-tile counters in the workspace (`ds` describes their layout).
+// in the workspace (`ds` describes their layout), summed by a second kernel.
 int gemm_tn_split(int T, int R, int C, const DwShape& ds, const uint8_t* G8, const uint8_t* X8, const float* sg,
-                  const float* sx, uint16_t* dW, int* counters, float* partials, DevStatus st, int sms,
+                  const float* sx, uint16_t* dW, float* partials, DevStatus st, int sms,
                   cudaStream_t s) {
   CUtensorMap tm_g, tm_x;
   bool ok = map2d(&tm_g, CU_TENSOR_MAP_DATA_TYPE_UINT8, G8, R, T, R, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -241,7 +234,6 @@ int gemm_tn_split(int T, int R, int C, const DwShape& ds, const uint8_t* G8, con
   wp.splits = choose_splits(pair_tiles, ds.kblocks_total, sms / wp.pair);
   wp.num_units = wp.splits * pair_tiles;
   wp.partials = partials;
-  wp.counters = counters;
   wp.dy_scale = sg;
   wp.x_scale = sx;
   wp.dW = dW;
@@ -499,8 +491,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* dyparts = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
-  int* dwcount = reinterpret_cast<int*>(wsb + kStatusBytes + 2 * kPartsBytes);
-  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes + dw_counter_bytes(dw_shape(dims)));
+  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes);
   const DevStatus st = dev_status(ws);
 
   BwdMaps m;
@@ -537,7 +528,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   rc = gemm_nt(T, D, N, dY8, W8T, dy_scale, w_scale, dx, st, sms, s);
   if (rc != QKVP_OK) return rc;
   // dW [N, D] = dY8^T . x8, both read MN-major
-  rc = gemm_tn_split(T, N, D, dw_shape(dims), dY8, x8, dy_scale, x_scale, dW, dwcount, dwparts, st, sms, s);
+  rc = gemm_tn_split(T, N, D, dw_shape(dims), dY8, x8, dy_scale, x_scale, dW, dwparts, st, sms, s);
   if (rc != QKVP_OK) return rc;
   return QKVP_OK;
 }
@@ -631,8 +622,7 @@ int qkvp_oproj_backward(int T, int D, int K, const uint16_t* dout, const uint8_t
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* gparts = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
   const DwShape ds = dw_shape_rc(D, K, T);
-  int* dwcount = reinterpret_cast<int*>(wsb + kStatusBytes + 2 * kPartsBytes);
-  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes + dw_counter_bytes(ds));
+  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes);
   const DevStatus st = dev_status(ws);
   rc = quantize_activation(dout, static_cast<int64_t>(T) * D, dout8, gparts, dout_scale, ws, s);
   if (rc != QKVP_OK) return rc;
@@ -640,7 +630,7 @@ int qkvp_oproj_backward(int T, int D, int K, const uint16_t* dout, const uint8_t
   rc = gemm_nt(T, K, D, dout8, Wo8T, dout_scale, wo_scale, da, st, sms, s);
   if (rc != QKVP_OK) return rc;
   // dWo [D, K] = dout8^T . a8, both read MN-major
-  return gemm_tn_split(T, D, K, ds, dout8, a8, dout_scale, a_scale, dWo, dwcount, dwparts, st, sms, s);
+  return gemm_tn_split(T, D, K, ds, dout8, a8, dout_scale, a_scale, dWo, dwparts, st, sms, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -652,12 +642,9 @@ int check_mlp(int T, int D, int F) {
   if (T > (1 << 24) || D % 128 || F % 128 || D > 16384 || F > 65536) return QKVP_ERR_UNSUPPORTED;
   return QKVP_OK;
 }
-// both weight gradients share the counters and partials (they run one after the other)
-size_t mlp_counter_bytes(int T, int D, int F) {
-  return std::max(dw_counter_bytes(dw_shape_rc(F, D, T)), dw_counter_bytes(dw_shape_rc(D, F, T)));
-}
+// both weight gradients share the partials (they run one after the other)
 size_t mlp_ws_bytes(int T, int D, int F) {
-  return kStatusBytes + 2 * kPartsBytes + mlp_counter_bytes(T, D, F) +
+  return kStatusBytes + 2 * kPartsBytes +
          std::max(dw_partial_bytes(dw_shape_rc(F, D, T), kMaxSplits), dw_partial_bytes(dw_shape_rc(D, F, T), kMaxSplits));
 }
 // h, dpre: bf16 intermediates quantised from the GEMM's own amax partials
@@ -726,8 +713,7 @@ int qkvp_mlp_backward(int T, int D, int F, const uint16_t* dout, const uint8_t* 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* parts_a = reinterpret_cast<float*>(wsb + kStatusBytes);
   float* parts_b = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
-  int* dwcount = reinterpret_cast<int*>(wsb + kStatusBytes + 2 * kPartsBytes);
-  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes + mlp_counter_bytes(T, D, F));
+  float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes);
   const DevStatus st = dev_status(ws);
   rc = quantize_activation(dout, static_cast<int64_t>(T) * D, dout8, parts_a, dout_scale, ws, s);
   if (rc != QKVP_OK) return rc;
@@ -742,11 +728,9 @@ int qkvp_mlp_backward(int T, int D, int F, const uint16_t* dout, const uint8_t* 
   rc = gemm_nt(T, D, F, dpre8, W1_8T, dpre_scale, w1_scale, dx, st, sms, s);
   if (rc != QKVP_OK) return rc;
   // dW1 [F, D] = dpre8^T . x8;  dW2 [D, F] = dout8^T . h8  (both operands MN-major)
-  rc = gemm_tn_split(T, F, D, dw_shape_rc(F, D, T), dpre8, x8, dpre_scale, x_scale, dW1, dwcount, dwparts, st, sms,
-                     s);
+  rc = gemm_tn_split(T, F, D, dw_shape_rc(F, D, T), dpre8, x8, dpre_scale, x_scale, dW1, dwparts, st, sms, s);
   if (rc != QKVP_OK) return rc;
-  return gemm_tn_split(T, D, F, dw_shape_rc(D, F, T), dout8, h8, dout_scale, h_scale, dW2, dwcount, dwparts, st,
-                       sms, s);
+  return gemm_tn_split(T, D, F, dw_shape_rc(D, F, T), dout8, h8, dout_scale, h_scale, dW2, dwparts, st, sms, s);
 }
 
 }  // extern "C"

@@ -5,7 +5,7 @@
 //   dX       acc = dY8 . W8         via W8T (K-major); epilogue: scale, bf16
 //   dW       acc = dY8^T . x8       MN-major operands straight from dY8 and x8,
 //                                   split over K (tokens); fp32 partials,
-//                                   reduced in a fixed order
+//                                   summed in split order by a second kernel
 //
 // One persistent, warp-specialised kernel body serves all three:
 //   warp 0     TMA producer: A tile (128 rows x 128 B of K) and B tile
@@ -680,7 +680,8 @@ __global__ void __launch_bounds__(gemm_threads(dx_epi_warps(MODE)), 1)
 }
 
 // ---------------------------------------------------------------------------
-// dW: split-K schedule, fp32 partial epilogue, fixed-order reduction.
+// dW: split-K schedule, fp32 partial epilogue; the partials are summed in
+// split order by dw_reduce_kernel, launched right after.
 // dW = dY8^T . x8 reads both operands MN-major straight from the token-major
 // tensors: a 128-token slice of dY8 [T, N] is the A tile (M = packed rows,
 // contiguous) and of x8 [T, D] the B tile (N = model columns, contiguous).
@@ -721,26 +722,20 @@ struct DwSched {
 
 // Epilogue of the dW GEMM.  Each unit stores its fp32 partial tile in the
 // layout [bn / 4][128 rows][4 columns], so that both the stores here and the
-// loads of the reduction are 16 bytes per lane and coalesced.  An epilogue
-// warp owns the same sub-tile (32 rows x bn / nsub columns) of every split of
-// a tile, and counts itself on that sub-tile's counter once its part of the
-// partial is stored; the warp that completes the count (the last split to
-// finish, in whatever order they finish) then sums the sub-tile's partials
-// over all splits in split order (the same sum, bit for bit, whichever warp
-// does it), scales by s_dy * s_x, writes it to dW in bf16 and resets the
-// counter for the next call.  No barrier spans warps, so a warp that leaves
-// early on an expired wait stalls no other.
+// loads of the reduction kernel are 16 bytes per lane and coalesced; an
+// epilogue warp stores one sub-tile (32 rows x bn / nsub columns).  (Summing
+// the splits here, in whichever warp stored a sub-tile's last split, left a
+// 10 us tail of dependent loads at the end of the kernel; a kernel of its own
+// spreads the sum over the whole GPU.)
 struct DwEpi {
   const DwParams& p;
   const DwSched& sc;
-  int qw, sub, nsub, lane, ew;
-  bool last;   // this warp completed its sub-tile of the unit just processed
+  int qw, sub, nsub, lane;
   __device__ void begin(int qw_, int sub_, int nsub_, int lane_, uint8_t*) {
     qw = qw_;
     sub = sub_;
     nsub = nsub_;
     lane = lane_;
-    ew = qw + 4 * sub;
   }
   __device__ void finish() {}
   __device__ void prepare(int) {}
@@ -751,7 +746,6 @@ struct DwEpi {
   __device__ static int quad(int c, int row) { return (c >> 2) * kBM + row; }
   template <class Release>
   __device__ void process(int u, uint32_t tacc, Release& release) {
-    last = false;
     // the odd CTA of the last pair may lie past the rows
     if (sc.mtile(u) >= p.m_tiles) return;
     const int row = qw * 32 + lane;
@@ -768,59 +762,8 @@ struct DwEpi {
                                                  __uint_as_float(raw[4 * i + 2]), __uint_as_float(raw[4 * i + 3]));
     }
     release();   // the accumulator is read
-    __threadfence();   // this lane's stores are visible device-wide before the count
-    __syncwarp();
-    int old = 0;
-    if (lane == 0) old = atomicAdd(p.counters + (sc.mtile(u) * p.n_tiles + sc.ntile(u)) * kDwEW + ew, 1);
-    last = __shfl_sync(0xffffffffu, old, 0) == p.splits - 1;
   }
-  __device__ void post(int u) {
-    if (!last) return;
-    __threadfence();
-    constexpr int QB = 4;   // column quads per batch
-    constexpr int SB = 4;   // splits per batch (their loads are all in flight together)
-    const int m = sc.mtile(u), nt = sc.ntile(u);
-    const int row = qw * 32 + lane, n = m * kBM + row;
-    const float scl = (*p.dy_scale) * (*p.x_scale);
-    const int share = p.bn / nsub;
-    const float4* src = reinterpret_cast<const float4*>(p.partials + tile_of(u, 0) * p.bn * kBM);
-    const int64_t split_stride = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.bn * kBM / 4;   // float4s
-    for (int c0 = sub * share; c0 < (sub + 1) * share; c0 += 4 * QB) {
-      float4 acc[QB];
-#pragma unroll
-      for (int q = 0; q < QB; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < p.splits; s0 += SB) {   // split order: the same sum on every run
-        float4 v[SB][QB];
-#pragma unroll
-        for (int j = 0; j < SB; ++j)
-          if (s0 + j < p.splits)
-#pragma unroll
-            for (int q = 0; q < QB; ++q) v[j][q] = __ldcg(src + (s0 + j) * split_stride + quad(c0 + 4 * q, row));
-#pragma unroll
-        for (int j = 0; j < SB; ++j)
-          if (s0 + j < p.splits)
-#pragma unroll
-            for (int q = 0; q < QB; ++q) {
-              acc[q].x += v[j][q].x;
-              acc[q].y += v[j][q].y;
-              acc[q].z += v[j][q].z;
-              acc[q].w += v[j][q].w;
-            }
-      }
-      if (n < p.N) {
-        uint32_t w[2 * QB];
-#pragma unroll
-        for (int q = 0; q < QB; ++q) {
-          w[2 * q] = pack_bf16x2(acc[q].x * scl, acc[q].y * scl);
-          w[2 * q + 1] = pack_bf16x2(acc[q].z * scl, acc[q].w * scl);
-        }
-        uint4* out = reinterpret_cast<uint4*>(p.dW + static_cast<int64_t>(n) * p.D + nt * p.bn + c0);
-        out[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        out[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-    }
-    if (lane == 0) p.counters[(m * p.n_tiles + nt) * kDwEW + ew] = 0;   // every split has counted
-  }
+  __device__ void post(int) {}
 };
 
 template <bool PAIR>
@@ -970,9 +913,68 @@ static cudaError_t launch_dw_t(const CUtensorMap& tmA, const CUtensorMap& tmB, c
                            gemm_smem_bytes(ring, kDwEW, 0), cache, nullptr, s, tmA, tmB, p, st, ring);
 }
 
+// Sum of the dW GEMM's split partials, in split order (the same sum on every
+// run), scaled by s_dy * s_x and stored as bf16.  A warp takes 8 rows x 8
+// column quads, a lane two quads of one row (all their splits' loads in
+// flight together): each load instruction reads four 128-byte runs (8
+// consecutive rows of one quad), each store 32 bytes of a row.
+__global__ void __launch_bounds__(256) dw_reduce_kernel(const __grid_constant__ DwParams p) {
+  constexpr int kMaxS = 4;   // splits whose loads are issued together
+  const int lane = threadIdx.x & 31;
+  const int qblocks = p.D / 32;                                   // 8-quad blocks along D
+  const int64_t tiles = static_cast<int64_t>((p.N + 7) / 8) * qblocks;
+  const float scl = (*p.dy_scale) * (*p.x_scale);
+  const int64_t split_stride = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.bn * kBM / 4;   // float4s
+  const float4* src = reinterpret_cast<const float4*>(p.partials);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < tiles; w += nwarps) {
+    const int n = static_cast<int>(w / qblocks) * 8 + (lane & 7);
+    if (n >= p.N) continue;
+    const int mt = n / kBM, row = n % kBM;
+    int64_t at[2];
+    int d[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      d[h] = (static_cast<int>(w % qblocks) * 8 + (lane >> 3) + 4 * h) * 4;
+      const int nt = d[h] / p.bn, c = d[h] % p.bn;
+      at[h] = (static_cast<int64_t>(mt) * p.n_tiles + nt) * p.bn * kBM / 4 + (c / 4) * kBM + row;
+    }
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int s0 = 0; s0 < p.splits; s0 += kMaxS) {
+      float4 v[kMaxS][2];
+#pragma unroll
+      for (int j = 0; j < kMaxS; ++j)
+        if (s0 + j < p.splits)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) v[j][h] = __ldcg(src + (s0 + j) * split_stride + at[h]);
+#pragma unroll
+      for (int j = 0; j < kMaxS; ++j)
+        if (s0 + j < p.splits)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            acc[h].x += v[j][h].x;
+            acc[h].y += v[j][h].y;
+            acc[h].z += v[j][h].z;
+            acc[h].w += v[j][h].w;
+          }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      *reinterpret_cast<uint2*>(p.dW + static_cast<int64_t>(n) * p.D + d[h]) =
+          make_uint2(pack_bf16x2(acc[h].x * scl, acc[h].y * scl), pack_bf16x2(acc[h].z * scl, acc[h].w * scl));
+  }
+}
+
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,
                            DevStatus st, cudaStream_t s) {
-  return p.pair == 2 ? launch_dw_t<true>(tmA, tmB, p, sms, st, s) : launch_dw_t<false>(tmA, tmB, p, sms, st, s);
+  cudaError_t e =
+      p.pair == 2 ? launch_dw_t<true>(tmA, tmB, p, sms, st, s) : launch_dw_t<false>(tmA, tmB, p, sms, st, s);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = static_cast<int64_t>((p.N + 7) / 8) * (p.D / 32);
+  const int64_t blocks = (tiles + 7) / 8;   // eight warps per block
+  const int grid = static_cast<int>(blocks < 8 * sms ? blocks : 8 * sms);
+  dw_reduce_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace qkvp

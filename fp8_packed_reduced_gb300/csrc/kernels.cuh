@@ -94,7 +94,7 @@ struct DxParams {
   const float* aux_scale;  // DRELU2: their scale
 };
 
-// Epilogue warps of the dW GEMM; each owns one counter per output tile.
+// Epilogue warps of the dW GEMM.
 constexpr int kDwEpiWarps = 8;
 // Epilogue warps of the dX-shaped GEMM per epilogue mode (the ReLU-squared
 // modes do more per element and take eight); each writes one amax partial in
@@ -105,7 +105,6 @@ struct DwParams {
   // num_units = splits * ceil(m_tiles / pair) * n_tiles; kblocks_total = ceil(T/128)
   int N, D, bn, m_tiles, n_tiles, pair, splits, num_units, kblocks_total;
   float* partials;    // [splits][m_tiles][n_tiles] tiles of [bn / 4][128][4] float32
-  int* counters;      // [m_tiles * n_tiles * kDwEpiWarps] splits finished per sub-tile; 0 between calls
   const float* dy_scale;
   const float* x_scale;
   uint16_t* dW;       // [N, D] bf16

@@ -71,10 +71,11 @@ const char* qkvp_status_string(int status);
 
 /* Bytes of scratch that qkvp_forward and qkvp_backward need for `dims`
  * (one workspace serves both).  0 if dims are unsupported.  The workspace
- * starts with the device status word and holds the dW GEMM's per-tile
- * completion counters, which every backward leaves at zero; zero it once
- * with qkvp_workspace_init before first use, and again after a device error
- * (a call that stopped early may leave counters set).  Calls sharing one
+ * starts with the device status word and the activation quantiser's grid
+ * barrier, which every call leaves ready for the next; zero it once with
+ * qkvp_workspace_init before first use, and again after a device error (a
+ * call that stopped early may leave the barrier mid-count).  It also holds
+ * the amax partials and the dW GEMM's split partials.  Calls sharing one
  * workspace must not overlap on the GPU. */
 size_t qkvp_workspace_bytes(const qkvp_dims* dims);
 
@@ -82,7 +83,7 @@ size_t qkvp_workspace_bytes(const qkvp_dims* dims);
  * shape is unsupported). */
 size_t qkvp_bank_workspace_bytes(int L, int D, int H, int d_qk, int d_v);
 
-/* Zero a workspace (status word, counters and all partial buffers).
+/* Zero a workspace (status word, grid barrier and all partial buffers).
  * ws: device. */
 int qkvp_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
@@ -245,7 +246,8 @@ int qkvp_set_wait_timeout_ns(uint64_t ns);
  * is being captured into a CUDA graph), so consecutive events bracket one
  * kernel each.  Order of the kernels: qkvp_quantize_bank: amax, quantise;
  * qkvp_forward: x amax + quantise (one kernel), forward GEMM; qkvp_backward: dY amax,
- * dY quantise, dX GEMM, dW GEMM (with its split reduction).  n = 0 disarms.  Not
+ * dY quantise, dX GEMM, dW GEMM and its split reduction (two kernels, one
+ * interval).  n = 0 disarms.  Not
  * thread-safe; meant for benchmarks. */
 int qkvp_set_timing_events(void* const* events, int n);
 

@@ -23,7 +23,10 @@
  *     the layout stated at its argument.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous on that stream and never synchronise with the host, except
- *     qkvp_poll_device_status.
+ *     qkvp_poll_device_status.  Calls may be captured into a CUDA graph; the
+ *     first call of each kind on a device sizes its launch grids from device
+ *     attribute and occupancy queries (cached afterwards), so make it once
+ *     before capturing.
  *   - Arguments are validated on the host before anything is launched; on
  *     failure nothing is launched and a qkvp_status other than QKVP_OK is
  *     returned.  No C++ exception crosses this ABI.

@@ -3,6 +3,7 @@
 // No call allocates device memory and none synchronises the host, except
 // qkvp_poll_device_status.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -65,13 +66,16 @@ bool map3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, u
 }
 
 int sm_count() {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64];   // per device, written once (any thread may race to write the same value)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev < 64 && cache[dev]) return cache[dev];
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < 64) cache[dev] = n;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -26,6 +26,8 @@
 // them by TMA while the other group computes.
 // Within a warp, lanes map to rows so that the 16-byte reads of a quarter
 // warp hit eight distinct 16-byte bank groups of the swizzled boxes.
+#include <atomic>
+
 #include "kernels.cuh"
 
 namespace qkvp {
@@ -364,15 +366,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------------------
 template <int DQK, bool QUANT>
 static cudaError_t launch_t(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s) {
-  static bool done[64] = {};
+  static std::atomic<bool> done[64];   // per device: the shared-memory opt-in is set
   const int smem = bwd_smem_bytes(DQK, QUANT);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !done[dev]) {
+  if (dev >= 64 || !done[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(bwd_epi_kernel<DQK, QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev < 64) done[dev] = true;
+    if (dev < 64) done[dev].store(true, std::memory_order_relaxed);
   }
   bwd_epi_kernel<DQK, QUANT><<<grid, kBwdThreads, smem, s>>>(m, p, st);
   return cudaGetLastError();

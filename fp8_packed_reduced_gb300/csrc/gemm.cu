@@ -25,6 +25,7 @@
 // the shared-memory traffic of B (written by TMA, read by the MMA).
 // Every wait is bounded (see mbar_wait); on expiry the kernel records
 // QKVP_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#include <atomic>
 #include <utility>
 
 #include "kernels.cuh"
@@ -780,21 +781,32 @@ __global__ void __launch_bounds__(gemm_threads(kDwEW), 1)
 // ---------------------------------------------------------------------------
 // Every GEMM kernel may use up to kSmemMax bytes of dynamic shared memory.
 template <class K>
-static cudaError_t set_smem_once(K kernel, bool (&done)[64]) {
+static cudaError_t set_smem_once(K kernel, std::atomic<bool> (&done)[64]) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && done[dev]) return cudaSuccess;
+  if (dev < 64 && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-  if (e == cudaSuccess && dev < 64) done[dev] = true;
+  if (e == cudaSuccess && dev < 64) done[dev].store(true, std::memory_order_relaxed);
   return e;
 }
 
 // Co-resident 2-CTA clusters of a kernel at a given shared-memory size,
-// queried once per (kernel, device, size).
+// queried once per (kernel, device, size): per device one word holding the
+// size (high half) and the count (low half), so that a reader never pairs
+// one call's size with another's count.
 struct ClusterCache {
-  int smem[64] = {};
-  int clusters[64] = {};
+  std::atomic<uint64_t> v[64];
+  int lookup(int dev, int smem) const {
+    if (dev >= 64) return 0;
+    const uint64_t w = v[dev].load(std::memory_order_relaxed);
+    return static_cast<int>(w >> 32) == smem ? static_cast<int>(w & 0xFFFFFFFFu) : 0;
+  }
+  void store(int dev, int smem, int clusters) {
+    if (dev < 64)
+      v[dev].store((static_cast<uint64_t>(static_cast<uint32_t>(smem)) << 32) | static_cast<uint32_t>(clusters),
+                   std::memory_order_relaxed);
+  }
 };
 
 // Persistent launch: one CTA per SM (at most one per unit), or for pairs one
@@ -818,16 +830,13 @@ static cudaError_t launch_persistent(void (*kernel)(KArgs...), bool pair, int un
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int clusters = dev < 64 && cache.smem[dev] == smem ? cache.clusters[dev] : 0;
+    int clusters = cache.lookup(dev, smem);
     if (clusters <= 0) {
       cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1));
       e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
       if (e != cudaSuccess) return e;
       if (clusters <= 0) return cudaErrorInvalidConfiguration;
-      if (dev < 64) {
-        cache.smem[dev] = smem;
-        cache.clusters[dev] = clusters;
-      }
+      cache.store(dev, smem, clusters);
     }
     grid = 2 * (units < clusters ? units : clusters);
   }
@@ -840,7 +849,7 @@ template <int DQK, bool PAIR>
 static cudaError_t launch_fwd_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBv,
                                 const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                                 int sms, DevStatus st, cudaStream_t s) {
-  static bool done[64] = {};
+  static std::atomic<bool> done[64];
   static ClusterCache cache;
   // B tiles: hq heads of q or k, or two heads of v (this CTA's half in a pair)
   const int brows = (p.hq * DQK > 2 * p.d_v ? p.hq * DQK : 2 * p.d_v) / p.pair;
@@ -874,7 +883,7 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
 template <bool PAIR, int MODE>
 static cudaError_t launch_dx_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tdx,
                                const DxParams& p, int sms, DevStatus st, cudaStream_t s, int* grid_used) {
-  static bool done[64] = {};
+  static std::atomic<bool> done[64];
   static ClusterCache cache;
   constexpr int EW = dx_epi_warps(MODE);
   const Ring ring = ring_for(p.bn / p.pair * kBK, EW, kDxEPB);
@@ -904,7 +913,7 @@ cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 template <bool PAIR>
 static cudaError_t launch_dw_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const DwParams& p, int sms,
                                DevStatus st, cudaStream_t s) {
-  static bool done[64] = {};
+  static std::atomic<bool> done[64];
   static ClusterCache cache;
   const Ring ring = ring_for(p.bn / p.pair * kBK, kDwEW, 0);
   cudaError_t e = set_smem_once(dw_gemm_kernel<PAIR>, done);

@@ -4,6 +4,7 @@
 //   x quantise    (codes of x, token-major)
 //   RoPE table, and the timeout self-test kernel.
 #include <algorithm>
+#include <atomic>
 
 #include "kernels.cuh"
 
@@ -170,13 +171,16 @@ __global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__
 }
 
 static int bank_sms() {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64];   // per device, written once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev < 64 && cache[dev]) return cache[dev];
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < 64) cache[dev] = n;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -193,18 +197,18 @@ cudaError_t launch_bank_amax(const BankArgs& a, float* partials, cudaStream_t s)
 // One block per tile while the tiles of all layers fit on the GPU at once;
 // beyond that each block takes several tiles of its layer (one wave).
 cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStream_t s) {
-  static int per_sm[64] = {};
+  static std::atomic<int> per_sm[64];   // per device, written once
   const int sms = bank_sms();
   if (sms <= 0) return cudaErrorInvalidDevice;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int resident = dev < 64 ? per_sm[dev] : 0;
+  int resident = dev < 64 ? per_sm[dev].load(std::memory_order_relaxed) : 0;
   if (resident <= 0) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, bank_quant_kernel, 256, 0);
     if (e != cudaSuccess) return e;
     if (resident < 1) return cudaErrorInvalidConfiguration;
-    if (dev < 64) per_sm[dev] = resident;
+    if (dev < 64) per_sm[dev].store(resident, std::memory_order_relaxed);
   }
   const int tiles = ((a.N + 127) / 128) * (a.D / 128);
   const int per_layer = std::max(1, std::min(tiles, resident * sms / a.L));
@@ -348,11 +352,11 @@ __global__ void __launch_bounds__(kFusedThreads) x_amax_quant_kernel(const uint1
 
 cudaError_t launch_x_amax_quant(const uint16_t* x, int64_t n, uint8_t* x8, float* partials, float* x_scale,
                                 GridBar* bar, DevStatus st, cudaStream_t s) {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64];   // per device, written once
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int blocks = dev < 64 ? cache[dev] : 0;
+  int blocks = dev < 64 ? cache[dev].load(std::memory_order_relaxed) : 0;
   if (blocks <= 0) {
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -361,7 +365,7 @@ cudaError_t launch_x_amax_quant(const uint16_t* x, int64_t n, uint8_t* x8, float
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     blocks = sms * per_sm < kMaxFusedBlocks ? sms * per_sm : kMaxFusedBlocks;
-    if (dev < 64) cache[dev] = blocks;
+    if (dev < 64) cache[dev].store(blocks, std::memory_order_relaxed);
   }
   // no more blocks than groups of 16 values (each block then has work in both steps)
   const int64_t n16 = n / 16;

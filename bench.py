@@ -70,10 +70,10 @@ def algorithmic_work(s: synth.Shape):
 KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu"}
 TRAFFIC = {
     "T": 24576,
-    "sources_sha256": {"bwd": "face1cd5cb074c3fb6aad4b811a42e499dd3737995633c33449127f2aa2b9d72", "gemm": "696a942e7bafcaa7610f102543805fc705bee9e83e4275130feb898ee32c6e79"},
+    "sources_sha256": {"bwd": "dfe7c1bb9b32051e09ed8bdbd973db66ca4bc7b64f1a4121b77e13eee85e4a55", "gemm": "a8e5973c0c9b9c5d9224d1b25ad9cc5732e13f9b71f559a2c93cb10a9b329e91"},
     # dw_gemm: the GEMM and its split-reduction kernel (one span)
-    "bytes": {"dy_amax": ("bwd", 158.71e6), "dy_quant": ("bwd", 179.65e6), "fwd_gemm": ("gemm", 64.15e6),
-              "dx_gemm": ("gemm", 52.51e6), "dw_gemm": ("gemm", 86.37e6)},
+    "bytes": {"dy_amax": ("bwd", 158.45e6), "dy_quant": ("bwd", 179.94e6), "fwd_gemm": ("gemm", 64.50e6),
+              "dx_gemm": ("gemm", 52.67e6), "dw_gemm": ("gemm", 86.34e6)},
 }
 
 

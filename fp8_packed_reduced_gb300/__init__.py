@@ -35,12 +35,16 @@ ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_INPUT = 4, 5, 6, 7
 
 
 class QKVPError(RuntimeError):
+    """A non-OK qkvp_status from a library call; ``code`` holds the status."""
+
     def __init__(self, code: int, where: str):
         self.code = code
         super().__init__(f"{where}: {STATUS.get(code, code)}")
 
 
 class Dims(ctypes.Structure):
+    """The C ``qkvp_dims`` struct."""
+
     _fields_ = [("T", ctypes.c_int), ("D", ctypes.c_int), ("H", ctypes.c_int),
                 ("d_qk", ctypes.c_int), ("d_v", ctypes.c_int)]
 
@@ -126,6 +130,9 @@ def _need_cuda(t: torch.Tensor, name: str, dtype=None, shape=None):
 
 @dataclass(frozen=True)
 class Shape:
+    """Problem shape of one layer: T tokens, model width D, H heads of
+    d_qk (q, k) and d_v (v) columns."""
+
     T: int
     D: int
     H: int
@@ -141,6 +148,7 @@ class Shape:
 
 
 def workspace_bytes(shape: Shape) -> int:
+    """Bytes of workspace forward/backward need for ``shape`` (0: unsupported)."""
     d = shape.dims()
     return int(lib().qkvp_workspace_bytes(ctypes.byref(d)))
 
@@ -171,6 +179,7 @@ def set_timing_events(events):
 
 
 def timing_events_recorded() -> int:
+    """Events the armed timing hook has recorded so far."""
     return int(lib().qkvp_timing_events_recorded())
 
 
@@ -184,10 +193,15 @@ def set_cta_pairs(mask: int) -> int:
 
 
 def set_wait_timeout_ns(ns: int):
+    """Limit of every device-side wait in the library's kernels (ns); a wait
+    that runs out records QKVP_ERR_TIMEOUT in the workspace's status word."""
     _check(lib().qkvp_set_wait_timeout_ns(ns), "qkvp_set_wait_timeout_ns")
 
 
 def selftest_wait_timeout(ws: torch.Tensor, timeout_us: int):
+    """Launch the self-test kernel whose bounded wait on a barrier that
+    nothing arrives on runs out after ``timeout_us`` and records
+    QKVP_ERR_TIMEOUT (the context stays usable)."""
     _check(lib().qkvp_selftest_wait_timeout(_ptr(ws), ws.numel(), timeout_us, _stream(ws.device)),
            "qkvp_selftest_wait_timeout")
 

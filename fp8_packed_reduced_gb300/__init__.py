@@ -218,6 +218,24 @@ def build_rope_table(max_pos: int, d_qk: int, base: float = 10000.0, device="cud
 # Bank refresh (once per optimizer update)
 # ----------------------------------------------------------------------------
 
+# Scratch of the weight refreshes, one per (device, stream): zeroed once when
+# it is made, and left zeroed by every refresh (the counters its kernel's
+# blocks share), so that refreshes on one stream reuse it and refreshes on
+# different streams never share one.
+_refresh_scratch = {}
+
+
+def _refresh_ws(dev, nbytes: int) -> torch.Tensor:
+    stream = torch.cuda.current_stream(dev)
+    key = (torch.device(dev).index, stream.cuda_stream)
+    ws = _refresh_scratch.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        _check(lib().qkvp_workspace_init(_ptr(ws), nbytes, _stream(ws.device)), "qkvp_workspace_init")
+        _refresh_scratch[key] = ws
+    return ws
+
+
 def quantize_bank(layers: Sequence[Sequence[torch.Tensor]], H: int, d_qk: int = 96, d_v: int = 128,
                   out=None):
     """Quantise L layers of (W_q, W_k, W_v) bf16 into the dual-layout FP8 bank.
@@ -242,10 +260,10 @@ def quantize_bank(layers: Sequence[Sequence[torch.Tensor]], H: int, d_qk: int = 
     nws = int(lib().qkvp_bank_workspace_bytes(L, D, H, d_qk, d_v))
     if nws == 0:
         raise QKVPError(ERR_UNSUPPORTED, "qkvp_bank_workspace_bytes")
-    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    ws = _refresh_ws(dev, nws)
     arr = lambda i: (ctypes.c_void_p * L)(*[ctypes.c_void_p(layers[l][i].data_ptr()) for l in range(L)])
     _check(lib().qkvp_quantize_bank(L, D, H, d_qk, d_v, arr(0), arr(1), arr(2), _ptr(W8), _ptr(W8T),
-                                    _ptr(w_scale), _ptr(ws), nws, _stream(dev)), "qkvp_quantize_bank")
+                                    _ptr(w_scale), _ptr(ws), ws.numel(), _stream(dev)), "qkvp_quantize_bank")
     return W8, W8T, w_scale
 
 
@@ -457,9 +475,9 @@ def quantize_weight(weights: Sequence[torch.Tensor], out=None):
     nws = int(lib().qkvp_weight_workspace_bytes(L, R, C))
     if nws == 0:
         raise QKVPError(ERR_UNSUPPORTED, "qkvp_weight_workspace_bytes")
-    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    ws = _refresh_ws(dev, nws)
     arr = (ctypes.c_void_p * L)(*[ctypes.c_void_p(w.data_ptr()) for w in weights])
-    _check(lib().qkvp_quantize_weight(L, R, C, arr, _ptr(W8), _ptr(W8T), _ptr(w_scale), _ptr(ws), nws,
+    _check(lib().qkvp_quantize_weight(L, R, C, arr, _ptr(W8), _ptr(W8T), _ptr(w_scale), _ptr(ws), ws.numel(),
                                       _stream(dev)), "qkvp_quantize_weight")
     return W8, W8T, w_scale
 

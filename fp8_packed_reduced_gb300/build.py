@@ -2,14 +2,20 @@
 
 Each CUDA translation unit is compiled by its own nvcc process (in parallel)
 and the objects are linked into ``fp8_packed_reduced_gb300/libqkvp.so``.
-Objects go to ``_build/`` at the repository root.  Incremental: a unit is
-recompiled only when it or a header is newer than its object.
+Objects go to ``_build/`` at the repository root.  Incremental, by content:
+each object and the library carry a stamp file with the SHA-256 of what they
+were built from (the unit's source, every header, the compiler flags, the
+nvcc version and the host machine type), and anything whose stamp does not
+match the current sources is rebuilt, whatever the files' times say.
 """
 
 from __future__ import annotations
 
 import concurrent.futures as cf
+import functools
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -23,6 +29,7 @@ LIB = os.path.join(PKG, "libqkvp.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
+LINK = ["-shared", "-cudart=static"]
 
 
 def nvcc() -> str:
@@ -36,17 +43,48 @@ def _sources():
     return sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _headers_mtime():
+def _headers():
     hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     hs += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
-    return max(os.path.getmtime(h) for h in hs)
+    return sorted(hs)
+
+
+@functools.lru_cache(maxsize=None)
+def _toolchain() -> str:
+    r = subprocess.run([nvcc(), "--version"], capture_output=True, text=True)
+    return r.stdout + platform.machine()
+
+
+def _digest(paths, extra) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    for e in extra:
+        h.update(b"\0" + str(e).encode())
+    h.update(_toolchain().encode())
+    return h.hexdigest()
+
+
+def _stamp_ok(target: str, digest: str) -> bool:
+    stamp = target + ".sha256"
+    if not (os.path.exists(target) and os.path.exists(stamp)):
+        return False
+    with open(stamp) as f:
+        return f.read().strip() == digest
+
+
+def _write_stamp(target: str, digest: str):
+    with open(target + ".sha256", "w") as f:
+        f.write(digest + "\n")
 
 
 def _compile(src: str, extra, verbose: bool) -> str:
     obj = os.path.join(BUILD, src[:-3] + ".o")
     srcp = os.path.join(CSRC, src)
-    fresh = os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(srcp), _headers_mtime())
-    if fresh and not extra:
+    digest = _digest([srcp, *_headers()], [*ARCH, *FLAGS, *extra])
+    if _stamp_ok(obj, digest) and not extra:
         return obj
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", srcp, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -54,6 +92,7 @@ def _compile(src: str, extra, verbose: bool) -> str:
         sys.stderr.write(r.stdout + r.stderr)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}")
+    _write_stamp(obj, digest)
     return obj
 
 
@@ -64,15 +103,17 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra, verbose or ptxas_info), srcs))
-    if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs):
+    digest = _digest(objs, [*ARCH, *LINK])
+    if _stamp_ok(LIB, digest):
         return LIB
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-cudart=static", "-o", tmp, *objs]
+    cmd = [nvcc(), *ARCH, *LINK, "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("linking libqkvp.so failed")
     os.replace(tmp, LIB)
+    _write_stamp(LIB, digest)
     return LIB
 
 

@@ -81,7 +81,9 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_dims(const qkvp_dims* d) {
+}  // namespace
+
+int qkvp::check_dims(const qkvp_dims* d) {
   if (!d) return QKVP_ERR_INVALID_ARGUMENT;
   if (d->T < 1 || d->D < 1 || d->H < 1 || d->d_qk < 1 || d->d_v < 1) return QKVP_ERR_INVALID_ARGUMENT;
   if (d->T > (1 << 24)) return QKVP_ERR_UNSUPPORTED;
@@ -91,6 +93,8 @@ int check_dims(const qkvp_dims* d) {
   if (d->d_v != 128) return QKVP_ERR_UNSUPPORTED;
   return QKVP_OK;
 }
+
+namespace {
 
 // Workspace: [status 256 B][x amax partials][dY amax partials][dW partials]
 constexpr size_t kStatusBytes = 256;
@@ -145,9 +149,11 @@ struct TimingHook {
   int n = 0, next = 0;
 } g_timing;
 
+}  // namespace
+
 // Recorded as an external event node when the stream is being captured into
 // a CUDA graph (so the graph's launches record it too), plainly otherwise.
-void mark(cudaStream_t s) {
+void qkvp::mark(cudaStream_t s) {
   if (g_timing.next >= g_timing.n) return;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   cudaStreamIsCapturing(s, &cs);
@@ -157,6 +163,8 @@ void mark(cudaStream_t s) {
   else
     cudaEventRecord(ev, s);
 }
+
+namespace {
 
 #define QKVP_TRY_CUDA(expr)                          \
   do {                                               \
@@ -272,7 +280,7 @@ size_t qkvp_workspace_bytes(const qkvp_dims* dims) {
 size_t qkvp_bank_workspace_bytes(int L, int D, int H, int d_qk, int d_v) {
   const qkvp_dims d{1, D, H, d_qk, d_v};
   if (L < 1 || L > kMaxLayers || check_dims(&d) != QKVP_OK) return 0;
-  return kStatusBytes + static_cast<size_t>(L) * kBankAmaxBlocks * sizeof(float);
+  return kStatusBytes + sizeof(BankSync);
 }
 
 int qkvp_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -358,12 +366,10 @@ int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v, const uint16_t* c
   a.D = D;
   a.Nq = H * d_qk;
   a.N = H * (2 * d_qk + d_v);
-  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  BankSync* sy = reinterpret_cast<BankSync*>(static_cast<uint8_t*>(ws) + kStatusBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   mark(s);
-  QKVP_TRY_CUDA(launch_bank_amax(a, partials, s));
-  mark(s);
-  QKVP_TRY_CUDA(launch_bank_quant(a, partials, s));
+  QKVP_TRY_CUDA(launch_bank_refresh(a, sy, dev_status(ws), s));
   mark(s);
   return QKVP_OK;
 }
@@ -542,7 +548,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
 // ---------------------------------------------------------------------------
 size_t qkvp_weight_workspace_bytes(int L, int R, int C) {
   if (L < 1 || L > kMaxLayers || R < 128 || C < 128 || R % 128 || C % 128 || R > 65536 || C > 16384) return 0;
-  return kStatusBytes + static_cast<size_t>(L) * kBankAmaxBlocks * sizeof(float);
+  return kStatusBytes + sizeof(BankSync);
 }
 
 int qkvp_quantize_weight(int L, int R, int C, const uint16_t* const* W, uint8_t* W8, uint8_t* W8T, float* w_scale,
@@ -567,12 +573,10 @@ int qkvp_quantize_weight(int L, int R, int C, const uint16_t* const* W, uint8_t*
   a.D = C;
   a.Nq = 0;
   a.N = R;
-  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  BankSync* sy = reinterpret_cast<BankSync*>(static_cast<uint8_t*>(ws) + kStatusBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   mark(s);
-  QKVP_TRY_CUDA(launch_bank_amax(a, partials, s));
-  mark(s);
-  QKVP_TRY_CUDA(launch_bank_quant(a, partials, s));
+  QKVP_TRY_CUDA(launch_bank_refresh(a, sy, dev_status(ws), s));
   mark(s);
   return QKVP_OK;
 }

@@ -8,6 +8,12 @@ namespace qkvp {
 
 constexpr int kMaxLayers = 128;
 
+// Host-side helpers of the C ABI shared by its translation units.
+// check_dims: QKVP_OK or the status the entry points return for `d`.
+int check_dims(const qkvp_dims* d);
+// mark: records the next armed timing event (qkvp_set_timing_events) on `s`.
+void mark(cudaStream_t s);
+
 // ---------------------------------------------------------------------------
 // Bank refresh
 // ---------------------------------------------------------------------------
@@ -20,10 +26,19 @@ struct BankArgs {
   float* w_scale;    // [L]
   int L, D, N, Nq;   // Nq = H * d_qk
 };
-constexpr int kBankAmaxBlocks = 32;   // partial maxima per layer
+// Counters of one bank refresh, in device memory that starts at zero; the
+// refresh kernel leaves them at zero when it completes.
+struct BankSync {
+  unsigned int next;               // work items claimed
+  unsigned int exited;             // blocks past their last item
+  unsigned int amax[kMaxLayers];   // per layer: bit pattern of max |w| so far
+  unsigned int done[kMaxLayers];   // per layer: amax items finished
+  unsigned int scale[kMaxLayers];  // per layer: bit pattern of the scale once known, else 0
+};
 
-cudaError_t launch_bank_amax(const BankArgs& a, float* partials, cudaStream_t s);
-cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStream_t s);
+// Amax and both code layouts of every layer in one launch (any grid size
+// works: blocks claim work items from the counters in `sy`).
+cudaError_t launch_bank_refresh(const BankArgs& a, BankSync* sy, DevStatus st, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Activation quantisation

@@ -1,5 +1,5 @@
 // Bandwidth-bound quantisation kernels:
-//   bank refresh  (amax per layer, then codes in both layouts from one pass)
+//   bank refresh  (amax per layer, then codes in both layouts, one launch)
 //   x amax        (per-tensor amax of the activations)
 //   x quantise    (codes of x, token-major)
 //   RoPE table, and the timeout self-test kernel.
@@ -52,45 +52,25 @@ cudaError_t launch_amax_bf16(const uint16_t* x, int64_t n, float* partials, int 
 }
 
 // ---------------------------------------------------------------------------
-// Bank refresh.  Pass 1: amax of each layer's logical Q/K/V packs, read in
-// place (no concatenation).  Pass 2: every block re-reduces its layer's
-// partials, then converts 128 x 128 tiles of the bank and writes each to both
-// W8 (row-major) and W8T (transposed) from the one read of that tile.  All
-// layers of a refresh go in one launch per pass, each sized to one wave; the
-// second pass reads the bank back from L2 for bank sizes that fit there.
+// Bank refresh in one launch.  The refresh is a list of work items over the
+// 128-row x 128-column tiles of all layers (layer by layer): items [0, U)
+// take the amax of tile i, items [U, 2U) convert tile i - U into both code
+// layouts.  Blocks claim items in order from a counter, so every amax item
+// is held by a running block before the first conversion item is handed
+// out: a block that waits for its layer's amax waits only on running blocks
+// that never wait themselves.  The launch therefore needs no co-residency
+// and may share the GPU with any other kernel.  An amax item folds its
+// tile's maximum into the layer's word (a max reduction on the bit pattern,
+// exact for non-negative floats) and then counts itself done; the block whose
+// count completes the layer publishes the layer's scale (before it can wait
+// on anything itself), and a conversion item waits (bounded) for that one
+// word, then converts its tile, read again (from L2 for banks that fit
+// there).  The last block out leaves the counters at zero for the next call.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ const uint16_t* bank_row(const BankArgs& a, int l, int n) {
   if (n < a.Nq) return a.Wq[l] + static_cast<int64_t>(n) * a.D;
   if (n < 2 * a.Nq) return a.Wk[l] + static_cast<int64_t>(n - a.Nq) * a.D;
   return a.Wv[l] + static_cast<int64_t>(n - 2 * a.Nq) * a.D;
-}
-
-// grid: (kBankAmaxBlocks, L), 1024 threads.  Block b of layer l takes a
-// contiguous band of rows; one warp per row, two rows in flight, the lanes
-// over the row's 16-byte chunks.
-__global__ void __launch_bounds__(1024) bank_amax_kernel(const __grid_constant__ BankArgs a, float* partials) {
-  __shared__ float red[32];
-  const int l = blockIdx.y;
-  const int cpr = a.D / 8;   // 16-byte chunks per row
-  const int band = (a.N + gridDim.x - 1) / gridDim.x;
-  const int r0 = blockIdx.x * band, r1 = min(a.N, r0 + band);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  float m = 0.f;
-  int n = r0 + warp;
-  for (; n + nw < r1; n += 2 * nw) {
-    const uint4* ra = reinterpret_cast<const uint4*>(bank_row(a, l, n));
-    const uint4* rb = reinterpret_cast<const uint4*>(bank_row(a, l, n + nw));
-#pragma unroll 4
-    for (int c = lane; c < cpr; c += 32)
-      m = fmaxf(m, fmaxf(absmax_bf16x8(__ldg(ra + c)), absmax_bf16x8(__ldg(rb + c))));
-  }
-  if (n < r1) {
-    const uint4* ra = reinterpret_cast<const uint4*>(bank_row(a, l, n));
-#pragma unroll 4
-    for (int c = lane; c < cpr; c += 32) m = fmaxf(m, absmax_bf16x8(__ldg(ra + c)));
-  }
-  m = block_max(m, red);
-  if (threadIdx.x == 0) partials[l * gridDim.x + blockIdx.x] = m;
 }
 
 // Transpose of a 4 x 4 byte block held as four row words: out[c] = bytes
@@ -104,115 +84,227 @@ __device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t 
   out[3] = __byte_perm(t1, t3, 0x7632);
 }
 
-// grid: (ceil(N/128) * D/128, L); 256 threads; tile 128 rows x 128 columns.
-// Thread t converts rows 4 (t / 8) .. + 3, columns 16 (t % 8) .. + 15 of the
-// tile: one 16-byte code store per row into W8, and, transposed in registers
-// by 4 x 4 byte blocks, sixteen 4-byte column words into a shared tile [128
-// columns][32 words of 4 rows], whose word index is XORed with 4 * (column /
-// 16) % 32 so that a warp's stores hit 32 banks; the tile then leaves as
-// 16-byte chunks of W8T rows.
-__global__ void __launch_bounds__(256) bank_quant_kernel(const __grid_constant__ BankArgs a,
-                                                         const float* partials) {
-  __shared__ float red[32];
-  __shared__ __align__(16) uint32_t tr[128][32];   // [tile column][row group, swizzled]
-  const int l = blockIdx.y;
-  const int tiles_d = a.D / 128;
-  const int tiles = (a.N + 127) / 128 * tiles_d;
-  const float amax = block_reduce_partials(partials + l * kBankAmaxBlocks, kBankAmaxBlocks, red);
-  const float s = scale_from_amax(amax);
-  const Bracket2 k = make_bracket2(s);
-  if (blockIdx.x == 0 && threadIdx.x == 0) a.w_scale[l] = s;
+// 16-byte read-only load with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ uint4 ldg_hint(const uint4* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
-  const int rg = threadIdx.x >> 3, cg = threadIdx.x & 7;
+constexpr int kBankThreads = 256;
+constexpr int kBankWarps = kBankThreads / 32;
+
+// Reductions without a returned value: max, and add with release semantics
+// (the thread's earlier writes and reductions are visible before the add).
+__device__ __forceinline__ void red_max_u32(unsigned int* p, unsigned int v) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Add that returns the old value, with acquire and release semantics.
+__device__ __forceinline__ unsigned int atom_add_acq_rel_u32(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void st_release_u32(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The count of an amax item of layer l returned `old` (acquire: every other
+// item's maximum of the layer is visible); if it completed the layer, the
+// layer's scale goes to w_scale and, released, to the published word.
+__device__ __forceinline__ void bank_publish_if_last(const BankArgs& a, BankSync* sy, int l, unsigned int old,
+                                                     unsigned int tpl) {
+  if (old != tpl - 1) return;
+  const float s = scale_from_amax(__uint_as_float(ld_relaxed_u32(&sy->amax[l])));
+  a.w_scale[l] = s;
+  st_release_u32(&sy->scale[l], __float_as_uint(s));   // s > 0: non-zero means published
+}
+
+// Tile of 128 bank rows x 128 columns.  Warp w, lane 16 h + j owns rows
+// n0 + 16 w + 8 h + i (i < 8) and columns d0 + 8 j .. + 7: each load
+// instruction of a half-warp reads one row's 256 contiguous bytes (two whole
+// 128-byte lines).  Rows at or past N read nothing.
+__device__ __forceinline__ void bank_load_tile(const BankArgs& a, int l, int n0, int d0, uint4 (&u)[8]) {
+  const int w = threadIdx.x >> 5, h = (threadIdx.x >> 4) & 1, j = threadIdx.x & 15;
+  const int nb = n0 + 16 * w + 8 * h;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    u[i] = nb + i < a.N ? __ldg(reinterpret_cast<const uint4*>(bank_row(a, l, nb + i) + d0 + 8 * j))
+                        : make_uint4(0, 0, 0, 0);
+}
+
+// Codes of a loaded tile into W8 (8 bytes per row and thread: a half-warp
+// writes one row's 128 contiguous bytes) and, transposed, into W8T.  Each
+// thread's 8 x 8 code block is transposed in registers; column col = 8 j + c
+// of the tile then holds the thread's 8 codes (rows 16 w + 8 h .. + 7) as one
+// 8-byte word, which goes to slot (2 w + h) ^ j of that column's 128-byte
+// line in shared memory (the XOR spreads a warp's stores over all banks),
+// and the lines leave as 16-byte chunks of W8T rows.
+__device__ __forceinline__ void bank_convert_tile(const BankArgs& a, int l, int n0, int d0, const uint4 (&u)[8],
+                                                  const Bracket2& kb, uint2 (*trT)[16]) {
+  const int w = threadIdx.x >> 5, h = (threadIdx.x >> 4) & 1, j = threadIdx.x & 15;
+  const int nb = n0 + 16 * w + 8 * h;
   uint8_t* W8 = a.W8 + static_cast<int64_t>(l) * a.N * a.D;
   uint8_t* W8T = a.W8T + static_cast<int64_t>(l) * a.N * a.D;
-  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {   // the layer's tiles, round-robin
-  const int n0 = (tile / tiles_d) * 128, d0 = (tile % tiles_d) * 128;
-  if (tile != static_cast<int>(blockIdx.x)) __syncthreads();   // the previous tile has left `tr`
-  uint4 code[4];   // the four rows' 16 codes
+  uint32_t lo[8], hi[8];   // codes of row i: columns 0-3, 4-7 of the thread's block
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int n = n0 + 4 * rg + i;
-    if (n < a.N) {
-      const uint4* src = reinterpret_cast<const uint4*>(bank_row(a, l, n) + d0 + 16 * cg);
-      const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-      const f2 v0[4] = {f2_from_bf16x2(u0.x), f2_from_bf16x2(u0.y), f2_from_bf16x2(u0.z), f2_from_bf16x2(u0.w)};
-      const f2 v1[4] = {f2_from_bf16x2(u1.x), f2_from_bf16x2(u1.y), f2_from_bf16x2(u1.z), f2_from_bf16x2(u1.w)};
-      const uint2 c0 = quant8(v0, k), c1 = quant8(v1, k);
-      code[i] = make_uint4(c0.x, c0.y, c1.x, c1.y);
-      *reinterpret_cast<uint4*>(W8 + static_cast<int64_t>(n) * a.D + d0 + 16 * cg) = code[i];
-    } else {
-      code[i] = make_uint4(0, 0, 0, 0);
-    }
+  for (int i = 0; i < 8; ++i) {
+    const f2 v[4] = {f2_from_bf16x2(u[i].x), f2_from_bf16x2(u[i].y), f2_from_bf16x2(u[i].z), f2_from_bf16x2(u[i].w)};
+    const uint2 c = quant8(v, kb);
+    if (nb + i < a.N) *reinterpret_cast<uint2*>(W8 + static_cast<int64_t>(nb + i) * a.D + d0 + 8 * j) = c;
+    lo[i] = c.x;
+    hi[i] = c.y;
   }
-  // column 16 cg + 4 q + c holds the bytes of rows 4 rg .. 4 rg + 3
-  const int sw = (cg & 7) << 2;
+  uint32_t t0[4], t1[4], t2[4], t3[4];
+  transpose4x4(lo[0], lo[1], lo[2], lo[3], t0);   // t0[c]: rows 0-3 of column c
+  transpose4x4(lo[4], lo[5], lo[6], lo[7], t1);   // t1[c]: rows 4-7 of column c
+  transpose4x4(hi[0], hi[1], hi[2], hi[3], t2);   // t2[c]: rows 0-3 of column 4 + c
+  transpose4x4(hi[4], hi[5], hi[6], hi[7], t3);
+  const int slot = (2 * w + h) ^ j;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t w[4];
-    const uint32_t* r = reinterpret_cast<const uint32_t*>(code);
-    transpose4x4(r[q], r[4 + q], r[8 + q], r[12 + q], w);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tr[16 * cg + 4 * q + c][rg ^ sw] = w[c];
+  for (int c = 0; c < 4; ++c) {
+    trT[8 * j + c][slot] = make_uint2(t0[c], t1[c]);
+    trT[8 * j + 4 + c][slot] = make_uint2(t2[c], t3[c]);
   }
   __syncthreads();
-  // W8T rows d0 .. d0 + 127, columns n0 .. n0 + 127 (N is a multiple of 64):
-  // chunk i (rows 16 i .. 16 i + 15 of the tile) of column col is the word
-  // group 4 i .. 4 i + 3, stored at 4 (i ^ (col / 16 % 8)).
-  const int nvalid = min(128, a.N - n0);
-  for (int e = threadIdx.x; e < 128 * 8; e += 256) {
-    const int col = e >> 3, i = e & 7;
-    if (16 * i < nvalid) {
-      const uint4 val = *reinterpret_cast<const uint4*>(&tr[col][4 * (i ^ ((col >> 4) & 7))]);
-      *reinterpret_cast<uint4*>(W8T + static_cast<int64_t>(d0 + col) * a.N + n0 + 16 * i) = val;
+  // chunk k (slots 2 k, 2 k + 1) of column col lies in the aligned slot pair
+  // at (2 k ^ (col / 8)) & ~1, its halves swapped when col / 8 is odd
+  const int nvalid = min(128, a.N - n0);   // a multiple of 64
+  for (int e = threadIdx.x; e < 128 * 8; e += kBankThreads) {
+    const int col = e >> 3, k = e & 7, jj = col >> 3;
+    if (16 * k < nvalid) {
+      uint4 v = *reinterpret_cast<const uint4*>(&trT[col][(2 * k ^ jj) & ~1]);
+      if (jj & 1) v = make_uint4(v.z, v.w, v.x, v.y);
+      *reinterpret_cast<uint4*>(W8T + static_cast<int64_t>(d0 + col) * a.N + n0 + 16 * k) = v;
     }
   }
+}
+
+// grid: resident blocks (at most one per tile), kBankThreads threads.
+__global__ void __launch_bounds__(kBankThreads, 4) bank_refresh_kernel(const __grid_constant__ BankArgs a,
+                                                                       BankSync* sy, DevStatus st) {
+  __shared__ __align__(16) uint2 trT[128][16];   // [tile column][8-row slot, swizzled]
+  __shared__ unsigned int claim[2];
+  __shared__ float scale_sh;
+  __shared__ float wmax[kBankWarps];
+  const int tiles_d = a.D / 128;
+  const int tpl = (a.N + 127) / 128 * tiles_d;              // tiles per layer
+  const unsigned int U = static_cast<unsigned int>(tpl * a.L);
+  const int lane = threadIdx.x & 31;
+  // thread 0: the count returned to this block's latest amax item, examined
+  // at the start of the block's next item (before any wait) or at the end
+  int pend_l = -1;
+  unsigned int pend_old = 0;
+  if (threadIdx.x == 0) claim[0] = atomicAdd(&sy->next, 1u);
+  __syncthreads();
+  for (int k = 0;; ++k) {
+    const unsigned int item = claim[k & 1];
+    if (item >= 2 * U) break;
+    // the next claim is in flight while this item runs (items only grow, so
+    // an amax item is never held behind a wait); its value is stored at the
+    // end of the item, so that no thread waits for it before then
+    unsigned int next_item = 0;
+    if (threadIdx.x == 0) next_item = atomicAdd(&sy->next, 1u);
+    const int tile = static_cast<int>(item < U ? item : item - U);
+    const int l = tile / tpl, lt = tile % tpl;
+    const int n0 = (lt / tiles_d) * 128, d0 = (lt % tiles_d) * 128;
+    uint4 u[8];
+    bank_load_tile(a, l, n0, d0, u);
+    // with this item's loads in flight, examine the previous amax item's
+    // count (it completes a layer at most once per layer; publishing here,
+    // before any wait, keeps the publication prompt)
+    if (threadIdx.x == 0 && pend_l >= 0) {
+      bank_publish_if_last(a, sy, pend_l, pend_old, tpl);
+      pend_l = -1;
+    }
+    if (item < U) {
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, absmax_bf16x8(u[i]));
+      m = warp_max(m);
+      if (lane == 0) wmax[threadIdx.x >> 5] = m;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float mm = wmax[0];
+#pragma unroll
+        for (int w = 1; w < kBankWarps; ++w) mm = fmaxf(mm, wmax[w]);
+        // the tile's maximum, then the count (released after the maximum)
+        red_max_u32(&sy->amax[l], __float_as_uint(mm));
+        pend_old = atom_add_acq_rel_u32(&sy->done[l], 1u);
+        pend_l = l;
+      }
+    } else {
+      // (the tile's loads are in flight while thread 0 waits for the scale)
+      if (threadIdx.x == 0) {
+        const int* word = reinterpret_cast<const int*>(&sy->scale[l]);
+        int sb = ld_acquire_gpu(word);
+        if (sb == 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while ((sb = ld_acquire_gpu(word)) == 0) {
+            __nanosleep(32);
+            if (globaltimer_ns() - t0 > st.timeout_ns) {
+              record_error(st, QKVP_ERR_TIMEOUT, KID_BANK_QUANT);
+              break;
+            }
+          }
+        }
+        scale_sh = __int_as_float(sb);   // 0 after a timeout: the tile is skipped
+      }
+      __syncthreads();
+      const float s = scale_sh;
+      if (s > 0.f) bank_convert_tile(a, l, n0, d0, u, make_bracket2(s), trT);
+    }
+    if (threadIdx.x == 0) claim[(k + 1) & 1] = next_item;
+    __syncthreads();   // the next claim is visible; `trT` and `scale_sh` are free again
+  }
+  if (threadIdx.x == 0) {
+    if (pend_l >= 0) bank_publish_if_last(a, sy, pend_l, pend_old, tpl);
+    __threadfence();
+    if (atomicAdd(&sy->exited, 1u) == gridDim.x - 1) {
+      // every block is past its last item and its last read of the counters
+      for (int l = 0; l < a.L; ++l) {
+        sy->amax[l] = 0u;
+        sy->done[l] = 0u;
+        sy->scale[l] = 0u;
+      }
+      sy->next = 0u;
+      sy->exited = 0u;
+      __threadfence();
+    }
   }
 }
 
-static int bank_sms() {
-  static std::atomic<int> cache[64];   // per device, written once
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev < 64) {
-    const int c = cache[dev].load(std::memory_order_relaxed);
-    if (c) return c;
-  }
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
-  return n;
-}
-
-// Up to 9 layers the amax grid fits the GPU in one wave of 1024-thread
-// blocks (two per SM); beyond that, blocks of 512 threads keep it to one.
-cudaError_t launch_bank_amax(const BankArgs& a, float* partials, cudaStream_t s) {
-  const int sms = bank_sms();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  const int threads = kBankAmaxBlocks * a.L <= 2 * sms ? 1024 : 512;
-  bank_amax_kernel<<<dim3(kBankAmaxBlocks, a.L), threads, 0, s>>>(a, partials);
-  return cudaGetLastError();
-}
-
-// One block per tile while the tiles of all layers fit on the GPU at once;
-// beyond that each block takes several tiles of its layer (one wave).
-cudaError_t launch_bank_quant(const BankArgs& a, const float* partials, cudaStream_t s) {
-  static std::atomic<int> per_sm[64];   // per device, written once
-  const int sms = bank_sms();
-  if (sms <= 0) return cudaErrorInvalidDevice;
+cudaError_t launch_bank_refresh(const BankArgs& a, BankSync* sy, DevStatus st, cudaStream_t s) {
+  static std::atomic<int> cache[64];   // per device: resident blocks, written once
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int resident = dev < 64 ? per_sm[dev].load(std::memory_order_relaxed) : 0;
+  int resident = dev < 64 ? cache[dev].load(std::memory_order_relaxed) : 0;
   if (resident <= 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, bank_quant_kernel, 256, 0);
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (resident < 1) return cudaErrorInvalidConfiguration;
-    if (dev < 64) per_sm[dev].store(resident, std::memory_order_relaxed);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bank_refresh_kernel, kBankThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    resident = sms * per_sm;
+    if (dev < 64) cache[dev].store(resident, std::memory_order_relaxed);
   }
-  const int tiles = ((a.N + 127) / 128) * (a.D / 128);
-  const int per_layer = std::max(1, std::min(tiles, resident * sms / a.L));
-  bank_quant_kernel<<<dim3(per_layer, a.L), 256, 0, s>>>(a, partials);
+  const int64_t tiles = static_cast<int64_t>((a.N + 127) / 128) * (a.D / 128) * a.L;
+  const int grid = static_cast<int>(tiles < resident ? tiles : resident);
+  bank_refresh_kernel<<<grid, kBankThreads, 0, s>>>(a, sy, st);
   return cudaGetLastError();
 }
 
@@ -261,11 +353,6 @@ cudaError_t launch_x_quant(const uint16_t* x, int64_t n, uint8_t* x8, const floa
 // ---------------------------------------------------------------------------
 // Grid barrier: every block's thread 0 arrives; the last to arrive resets the
 // count and advances the generation, the others wait (bounded) for that.
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void grid_barrier(GridBar* bar, const DevStatus& st, int kid) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -290,15 +377,6 @@ __device__ __forceinline__ void grid_barrier(GridBar* bar, const DevStatus& st, 
 }
 
 constexpr int kFusedThreads = 512;
-
-// 16-byte read-only load with an L2 eviction-priority policy (createpolicy).
-__device__ __forceinline__ uint4 ldg_hint(const uint4* ptr, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr), "l"(pol));
-  return v;
-}
 
 __global__ void __launch_bounds__(kFusedThreads) x_amax_quant_kernel(const uint16_t* __restrict__ x, int64_t n16,
                                                                      uint8_t* __restrict__ x8, float* partials,

@@ -83,7 +83,11 @@ const char* qkvp_status_string(int status);
 size_t qkvp_workspace_bytes(const qkvp_dims* dims);
 
 /* Bytes of scratch that qkvp_quantize_bank needs for L layers (0 if the
- * shape is unsupported). */
+ * shape is unsupported).  The scratch holds the status word and the
+ * counters the refresh kernel's blocks share; zero it once with
+ * qkvp_workspace_init before first use (every refresh leaves it zeroed),
+ * and again after a device error.  Refreshes sharing one scratch must not
+ * overlap on the GPU. */
 size_t qkvp_bank_workspace_bytes(int L, int D, int H, int d_qk, int d_v);
 
 /* Zero a workspace (status word, grid barrier and all partial buffers).
@@ -117,7 +121,14 @@ int qkvp_build_rope_table(float* table, int max_pos, int d_qk, double base, void
  *                concat(W_q, W_k, W_v)
  *   W8T          out, device, [L, D, N] codes, W8T[l] = transpose(W8[l])
  *   w_scale      out, device, [L] float32, one scale per layer (whole bank)
- *   ws           device scratch of qkvp_bank_workspace_bytes(...) bytes      */
+ *   ws           device scratch of qkvp_bank_workspace_bytes(...) bytes,
+ *                zeroed once (see qkvp_bank_workspace_bytes)
+ * One launch: blocks claim work items (the amax of a 128 x 128 tile, then
+ * the codes of a tile) in order from a counter in ws, so the launch needs no
+ * particular number of resident blocks and may run beside any other kernel;
+ * the code items of a layer wait (bounded, QKVP_ERR_TIMEOUT in the status
+ * word) until its amax items are done.  The second read of a tile comes from
+ * L2 for banks that fit there, so HBM sees one read of the weights. */
 int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v,
                        const uint16_t* const* Wq, const uint16_t* const* Wk,
                        const uint16_t* const* Wv,
@@ -128,18 +139,23 @@ int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v,
  * device memory (no cudaMalloc of their own, no workspace to hand over: for
  * example code confined to a framework's memory pool, or a refresh issued
  * where an allocation could block).  The pages have no counterpart: this is a
- * variant of qkvp_quantize_bank whose scratch (the per-layer partial maxima)
- * lives in a fixed 16 KB array of device memory inside this library, held by
- * every GPU that loads the library until the process exits.
- *   Arguments and results: as qkvp_quantize_bank, without ws/ws_bytes.
+ * variant of qkvp_quantize_bank whose scratch (a status word, the counters
+ * and per-layer maxima its blocks share) lives in a fixed 2 KB array of
+ * device memory inside this library, held by every GPU that loads the
+ * library until the process exits.
+ *   Arguments and results: as qkvp_quantize_bank, without ws/ws_bytes; bad
+ *   arguments give the same status as there.
  *   L above 128 is rejected with QKVP_ERR_UNSUPPORTED (the array's capacity).
- *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
- *   Every call shares the one array, which keeps the previous call's
- *   contents (nothing in it needs to start at zero).  Calls whose kernels
- *   overlap on the GPU (different streams, or different host threads) race
- *   on it: serialise them. */
+ *   The first call in a device's context looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current, and again after the
+ *   context was re-created; make that first call before any stream capture.
+ *   Every call shares the one array and clears its status word and counters
+ *   (cudaMemsetAsync on `stream`) before its kernel, so nothing is left over
+ *   from the previous call.  Calls whose kernels overlap on the GPU
+ *   (different streams, or different host threads) race on it: serialise
+ *   them.  A device-side wait that runs out (QKVP_ERR_TIMEOUT) is recorded
+ *   in the array's own status word, which no poll reads: the refresh's wait
+ *   depends only on blocks that are already running. */
 int qkvp_quantize_bank_static(int L, int D, int H, int d_qk, int d_v,
                               const uint16_t* const* Wq, const uint16_t* const* Wk,
                               const uint16_t* const* Wv,
@@ -212,7 +228,7 @@ int qkvp_forward_quantized(const qkvp_dims* dims, float eps,
  *   dx = (dY8 . W8) * s_dy * s_w   with the cached W8T as the K-major operand
  *   dW = (dY8^T . x8) * s_dy * s_x with dY8 and x8 read as MN-major operands,
  *        split over tokens; the split partials (fp32, in ws) are summed in
- *        split order by the GEMM itself, so dW is the same on every run
+ *        split order by a kernel of their own, so dW is the same on every run
  *   dq, dk    in  [H, T, d_qk] bf16     dv in [H, T, d_v] bf16
  *   q, k      in  [H, T, d_qk] bf16 saved forward outputs
  *   rstd      in  [2, H, T] float32 saved forward output
@@ -279,7 +295,8 @@ int qkvp_set_cta_pairs(int mask);
  * ------------------------------------------------------------------------ */
 
 /* Bytes of scratch qkvp_quantize_weight needs for L matrices [R, C] (0 if
- * unsupported: R, C multiples of 128, R <= 65536, C <= 16384, L <= 128). */
+ * unsupported: R, C multiples of 128, R <= 65536, C <= 16384, L <= 128).
+ * Zero it once with qkvp_workspace_init (every refresh leaves it zeroed). */
 size_t qkvp_weight_workspace_bytes(int L, int R, int C);
 
 /* Refresh of L weight matrices, once per optimizer update: one scale per

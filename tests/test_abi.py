@@ -109,6 +109,32 @@ def test_bank_validation_codes(qk):
     assert f(L, 768, 6, 96, 128, arr, arr, arr, p, p, p, p, 8, None) == qk.ERR_WORKSPACE_TOO_SMALL
 
 
+def test_static_bank_refresh_validates_like_the_workspace_one(qk):
+    """The allocation-free bank refresh rejects bad arguments with the same
+    status as qkvp_quantize_bank (both run the same host checks, before any
+    CUDA call)."""
+    L = 2
+    arr = (ctypes.c_void_p * L)(ctypes.c_void_p(4096), ctypes.c_void_p(4096))
+    mis = (ctypes.c_void_p * L)(ctypes.c_void_p(4096), ctypes.c_void_p(4098))
+    p = ctypes.c_void_p(4096)
+    lib = qk.lib()
+    bad = [
+        (0, 768, 6, 96, 128, arr),       # no layers
+        (L, 768, 6, 72, 128, arr),       # unsupported d_qk
+        (L, 768, 6, 0, 128, arr),        # non-positive d_qk
+        (L, 768, 6, 96, 0, arr),         # non-positive d_v
+        (L, 768, 6, 96, 64, arr),        # unsupported d_v
+        (L, 700, 6, 96, 128, arr),       # D not a multiple of 128
+        (L, 768, 0, 96, 128, arr),       # no heads
+        (L, 768, 200, 96, 128, arr),     # too many heads
+        (L, 768, 6, 96, 128, mis),       # a misaligned weight
+    ]
+    for L_, D, H, dqk, dv, a in bad:
+        ws_rc = lib.qkvp_quantize_bank(L_, D, H, dqk, dv, a, a, a, p, p, p, p, 1 << 20, None)
+        st_rc = lib.qkvp_quantize_bank_static(L_, D, H, dqk, dv, a, a, a, p, p, p, None)
+        assert ws_rc == st_rc != qk.OK, (L_, D, H, dqk, dv)
+
+
 def test_other_validation_codes(qk):
     lib = qk.lib()
     assert lib.qkvp_build_rope_table(None, 128, 96, 10000.0, None) == qk.ERR_INVALID_ARGUMENT

@@ -17,8 +17,7 @@ def test_algorithmic_work_at_the_training_shape():
     T, D, H, N = 49152, 768, 6, 1920
     # the packed output width: H heads of 96 + 96 + 128 columns
     assert TRAIN.N == N
-    assert w["bank_amax"] == ("hbm", N * D * 2)                        # one bf16 read of the bank
-    assert w["bank_quant"] == ("hbm", N * D * 2 + 2 * N * D)           # + both code layouts
+    assert w["bank_refresh"] == ("hbm", N * D * 2 + 2 * N * D)         # one bf16 read, both code layouts
     assert w["x_quant"] == ("hbm", 2 * T * D * 2 + T * D)              # x twice, x8 once
     for g in ("fwd_gemm", "dx_gemm", "dw_gemm"):
         assert w[g] == ("tensor", 2.0 * T * D * N)                     # 144.96 GFLOP each
@@ -34,10 +33,11 @@ def test_algorithmic_work_at_the_training_shape():
 
 
 def test_kernel_table_fractions():
-    peaks = dict(hbm=6000.0, bf16=2000.0, bf16_sus=1500.0)
+    peaks = dict(hbm=6000.0, bf16=1500.0, bf16_sus=1200.0)
     work = {"a": ("hbm", 6.0e9), "b": ("tensor", 3.0e12)}
     # 1 ms for 6 GB = 6000 GB/s (the whole HBM peak); 3 TFLOP in 1 ms = 3000
-    # TFLOP/s against the E4M3 peak of 2 x 1500
+    # TFLOP/s against the E4M3 peak of 2 x 1500 (the burst bf16 figure: the
+    # timed regions last milliseconds)
     kt = bench.kernel_table({"a": 1.0, "b": 1.0}, work, peaks)
     assert kt["a"]["unit"] == "GB/s" and kt["a"]["achieved"] == pytest.approx(6000.0)
     assert kt["a"]["frac"] == pytest.approx(1.0)

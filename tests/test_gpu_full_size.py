@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from helpers import assert_close, assert_codes_match
+from helpers import assert_chain_close, assert_close, assert_codes_match
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 f32 = synth.to_numpy_f32
@@ -85,6 +85,14 @@ def test_backward_full_codes_and_sampled_gradients(run):
     assert_close(f32(r["dx"][ROWS]), dYh @ oracle.dequantize(oW8, os_w), "dx")
     _, dW = oracle.grad_gemms(dY8, np.float32(r["dy_scale"]), oW8, os_w, x8, np.float32(r["x_scale"]))
     assert_close(f32(r["dW"]), dW, "dW")
+    # and the whole chain from the oracle's own codes and scale: dX on the
+    # sampled rows, dW in full (see assert_chain_close)
+    agree = bool(np.array_equal(dY8, dY8_ref))
+    dYh_ref = oracle.dequantize(dY8_ref[ROWS], s_dy)
+    assert_chain_close(f32(r["dx"][ROWS]), dYh_ref @ oracle.dequantize(oW8, os_w), "dx (oracle's own codes)",
+                       bool(np.array_equal(dY8[ROWS], dY8_ref[ROWS])))
+    _, dW_ref = oracle.grad_gemms(dY8_ref, s_dy, oW8, os_w, x8, np.float32(r["x_scale"]))
+    assert_chain_close(f32(r["dW"]), dW_ref, "dW (oracle's own codes)", agree)
 
 
 def test_backward_repeatable(run):

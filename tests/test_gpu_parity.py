@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from helpers import assert_close, assert_codes_match
+from helpers import assert_chain_close, assert_close, assert_codes_match
 
 pytestmark = pytest.mark.gpu
 
@@ -199,17 +199,33 @@ def _check_backward(qk, s):
     rank_one = s.T == 1      # dW is an outer product: see assert_close
     assert_close(f32(out["dx"]), dX, "dx (GPU codes)")
     assert_close(f32(out["dW"]), dW, "dW (GPU codes)", bf16_rounding=rank_one)
-    # The whole chain against the oracle's own codes.  Where a dY value sits
-    # within float32 rounding of an E4M3 tie, both codes are correct results;
-    # with one such code among few tokens a whole dW row moves by a grid step,
-    # so this comparison is made when the codes agree everywhere.
-    if np.array_equal(dY8, bw["dY8"]):
-        assert_close(f32(out["dx"]), bw["dX"], "dx")
-        assert_close(f32(out["dW"]), bw["dW"], "dW", bf16_rounding=rank_one)
+    # The whole chain against the oracle's own codes (see assert_chain_close:
+    # codes on either side of an E4M3 tie are both correct results).
+    agree = bool(np.array_equal(dY8, bw["dY8"]))
+    assert_chain_close(f32(out["dx"]), bw["dX"], "dx (oracle's own codes)", agree)
+    assert_chain_close(f32(out["dW"]), bw["dW"], "dW (oracle's own codes)", agree, bf16_rounding=rank_one)
 
 
 @pytest.mark.parametrize("s", SHAPES, ids=IDS)
 def test_backward_matches_oracle(qk, s):
+    _check_backward(qk, s)
+
+
+# The remaining points of the width / scale sweep (d_qk in {64, 96, 128},
+# D in {768, 1024, 2048}, H = D / 128) that the shapes above do not cover,
+# each with a ragged token tail: forward and backward against the oracle.
+SWEEP_SHAPES = [
+    synth.Shape(T=260, D=768, H=6, d_qk=64, d_v=128, seq_len=256),
+    synth.Shape(T=260, D=768, H=6, d_qk=128, d_v=128, seq_len=256),
+    synth.Shape(T=260, D=1024, H=8, d_qk=96, d_v=128, seq_len=256),
+    synth.Shape(T=260, D=2048, H=16, d_qk=64, d_v=128, seq_len=256),
+    synth.Shape(T=260, D=2048, H=16, d_qk=128, d_v=128, seq_len=256),
+]
+
+
+@pytest.mark.parametrize("s", SWEEP_SHAPES, ids=[f"T{s.T}_D{s.D}_H{s.H}_dqk{s.d_qk}" for s in SWEEP_SHAPES])
+def test_sweep_points_match_oracle(qk, s):
+    _check_forward(qk, s)
     _check_backward(qk, s)
 
 

@@ -62,11 +62,11 @@ def algorithmic_work(s: synth.Shape):
     }
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from the
-# ncu captures summarised in profiles/ncu_*_T24576_D768.md, taken at T = 24576
-# and scaled to the workload by its tokens.  Each figure describes the device
-# code of its kernel as it was captured (the digest of the kernel's source
-# file and the shared device headers) and is reported as null for any other.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
+# ncu captures of the kernels, taken at T = TRAFFIC["T"] tokens and scaled to
+# the workload by its tokens.  Each figure describes the device code of its
+# kernel as it was captured (the digest of the kernel's source file and the
+# shared device headers) and is reported as null for any other.
 KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu"}
 TRAFFIC = {
     "T": 24576,
@@ -368,6 +368,8 @@ def run_ours(args, rank, world):
     if not args.no_next_rows:
         line["bank_refresh"] = run_bank_refresh(args, dev, load_peaks())
         line["next_rows"] = {"oproj": run_oproj(args, dev, world), "mlp": run_mlp(args, dev, world)}
+    if not args.no_sweep:
+        line["sweep"] = run_sweep(args, dev, world)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, args.cpu_sample)
     return line
@@ -508,6 +510,56 @@ def run_mlp(args, dev, world):
             "steps": steps, "kernels": kern, "gpu_launches": (len(MLP_KERNELS) + 2) * steps}
 
 
+def run_sweep(args, dev, world, steps=20):
+    """The width / scale sweep: the whole step (bank refresh, forward,
+    backward) at T tokens for d_qk in {64, 96, 128} (d_v = 128: 256, 320 and
+    384 packed columns per head) and D in {768, 1024, 2048} with H = D / 128,
+    each timed as `steps` steps replayed from one CUDA graph.  Per D, the
+    step-time ratios of the reduced widths against the 384-column layout are
+    reported beside the column-count ratios (the work the GEMMs do scales with
+    the columns; the bandwidth-bound passes read and write the q, k, v and dY
+    columns)."""
+    points = []
+    for D in (768, 1024, 2048):
+        for dqk in (64, 96, 128):
+            s = synth.Shape(T=args.T, D=D, H=D // 128, d_qk=dqk, d_v=128, seq_len=args.seq_len)
+            st = Step(s, dev)
+            stream = torch.cuda.Stream(dev)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    st.step()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(steps):
+                    st.step()
+            graph.replay()
+            torch.cuda.synchronize()
+            cur = torch.cuda.current_stream(dev)   # the stream the replays run on
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            graph.replay()
+            b.record(cur)
+            torch.cuda.synchronize()
+            code, where = st.qk.poll_device_status(st.ws)
+            if code != 0:
+                raise RuntimeError(f"device status {st.qk.STATUS.get(code)} from kernel {where}")
+            ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+            flops = 3 * 2.0 * s.T * s.D * s.N
+            points.append({"D": D, "H": s.H, "d_qk": dqk, "cols_per_head": 2 * dqk + 128,
+                           "ms_per_step": round(ms, 5), "tokens_per_s": round(job_tokens_per_s(s.T, world, ms), 1),
+                           "gemm_tflops_per_step": round(flops / (ms * 1e-3) / 1e12, 1)})
+            del graph, st
+            torch.cuda.empty_cache()
+    ratios = []
+    for D in (768, 1024, 2048):
+        t = {p_["d_qk"]: p_["ms_per_step"] for p_ in points if p_["D"] == D}
+        ratios.append({"D": D, "t320_over_t384": round(t[96] / t[128], 4), "cols_320_over_384": round(320 / 384, 4),
+                       "t256_over_t384": round(t[64] / t[128], 4), "cols_256_over_384": round(256 / 384, 4)})
+    return {"workload": f"whole step at T={args.T}: d_qk in 64/96/128 (d_v 128), D in 768/1024/2048, H = D/128",
+            "steps_per_point": steps, "points": points, "ratios": ratios}
+
+
 def run_bank_refresh(args, dev, peaks, L=12, copies=8, repeats=32):
     """The weight-bank workload: L layers of the packed bank [N, D] refreshed
     from their bf16 sources in one call (amax, then both code layouts),
@@ -527,20 +579,22 @@ def run_bank_refresh(args, dev, peaks, L=12, copies=8, repeats=32):
         banks.append(synth.bank_layers(L, H, D, dqk, dv, perturb=1e-3 if c % 2 else 0.0, device=dev))
         outs.append((torch.empty((L, N, D), **u8), torch.empty((L, D, N), **u8),
                      torch.empty((L,), dtype=torch.float32, device=dev)))
-    for c in range(copies):          # warm-up, and the scratch made before capture
-        qk.quantize_bank(banks[c], H, dqk, dv, out=outs[c])
+    stream = torch.cuda.Stream(dev)    # warm-up and capture on one stream: its scratch is made before capture
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            qk.quantize_bank(banks[c], H, dqk, dv, out=outs[c])
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream(dev)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for r in range(repeats):
             qk.quantize_bank(banks[r % copies], H, dqk, dv, out=outs[r % copies])
     graph.replay()
     torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)   # the stream the replays run on
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(cur)
     graph.replay()
-    b.record(stream)
+    b.record(cur)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / repeats
     moved = L * (N * D * 2 + 2 * N * D)   # bf16 sources read once, both code layouts written
@@ -690,6 +744,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the bank-refresh, output-projection and MLP measurements")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the width / scale sweep")
     ap.add_argument("--cta-pairs", type=int, default=None,
                     help="GEMMs on 2-CTA clusters: bit 0 forward, bit 1 dX, bit 2 dW (default: the library's)")
     args = ap.parse_args()

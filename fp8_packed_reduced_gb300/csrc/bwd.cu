@@ -25,7 +25,11 @@
 // ahead.  Pass 2 stages the codes of its unit (32-byte swizzle) and stores
 // them by TMA while the other group computes.
 // Within a warp, lanes map to rows so that the 16-byte reads of a quarter
-// warp hit eight distinct 16-byte bank groups of the swizzled boxes.
+// warp hit eight distinct 16-byte bank groups of the swizzled boxes.  In
+// pass 1 the group's threads meet only through mbarriers (a stage landed;
+// all have read a stage), so its warps may run apart by up to the ring's
+// depth; pass 2 also meets at a group barrier per unit, before its single
+// code staging is rewritten.
 #include <atomic>
 
 #include "kernels.cuh"
@@ -128,7 +132,6 @@ __device__ __forceinline__ bool group_all(int g, bool v) {
   return out != 0;
 }
 
-
 // One kernel body for both passes.  QUANT = false: amax partials; true: codes.
 template <int DQK, bool QUANT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -141,9 +144,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[2 * kMaxStagesPerGroup];
-  // per group: every thread of the group is done with its current stage (and,
-  // in pass 2, has staged its codes); the group's thread 0 waits on it alone
-  __shared__ __align__(8) uint64_t done[2];
+  // per group and stage: every thread of the group is done with the stage's
+  // current unit (and, in pass 2, has staged its codes); the group's thread 0
+  // waits on it alone.  One barrier per stage: a thread that runs ahead can
+  // only arrive again on a stage after thread 0 has refilled it, which it
+  // does once the earlier phase has completed.
+  __shared__ __align__(8) uint64_t done[2][kMaxStagesPerGroup];
   __shared__ float red[32];
   __shared__ int abort_flag;
   const int g = threadIdx.x / kGroupThreads;    // consumer group
@@ -154,7 +160,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < 2 * SPG; ++s) mbar_init(&full[s], 1);
-    for (int gg = 0; gg < 2; ++gg) mbar_init(&done[gg], kGroupThreads);
+    for (int gg = 0; gg < 2; ++gg)
+      for (int s = 0; s < SPG; ++s) mbar_init(&done[gg][s], kGroupThreads);
     fence_mbar_init();
   }
   __syncthreads();
@@ -259,10 +266,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BwdUnit bn = bwd_decode(p, un);
       if (bn.part < 2) row_state(p, bn, bn.t0 + r, rstd_next, pos_next);
     }
-    // (pass 2: thread 0 first lets the previous unit's codes leave the
-    // staging, which this unit overwrites after the barrier)
-    if (QUANT && gt == 0) bulk_wait_read<0>();
-    if (!group_all(g, mbar_wait(&gfull[s], par, &abort_flag, st, kid) && !abort_flag)) break;
+    if (QUANT) {
+      // pass 2: thread 0 first lets the previous unit's codes leave the
+      // staging, which this unit overwrites after the group barrier (the
+      // staging is single: the group meets at every unit)
+      if (gt == 0) bulk_wait_read<0>();
+      if (!group_all(g, mbar_wait(&gfull[s], par, &abort_flag, st, kid) && !abort_flag)) break;
+    } else {
+      // pass 1: each thread waits for the stage itself, so the group's warps
+      // run apart by up to the ring's depth instead of meeting at every unit
+      if (!mbar_wait(&gfull[s], par, &abort_flag, st, kid) || abort_flag) break;
+    }
     if (gt == 0) inflight &= ~(1u << s);
     const uint8_t* in0 = stages + s * kStage;
     int nbox;
@@ -340,8 +354,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // the TMA store first.  Thread 0 alone waits for the whole group, then
     // refills the stage and stores the codes.
     if (QUANT) fence_async_smem();
-    mbar_arrive(&done[g]);
-    if (gt == 0 && mbar_wait(&done[g], k & 1, &abort_flag, st, kid)) {
+    mbar_arrive(&done[g][s]);
+    if (gt == 0 && mbar_wait(&done[g][s], par, &abort_flag, st, kid)) {
       if (unit_at(k + SPG) >= 0) load_unit(unit_at(k + SPG), s, par ^ 1u);
       if (QUANT) {
         for (int j = 0; j < nbox; ++j) tma_store_2d(&m.dy8, out8 + j * kOutBox, b.col0 + 32 * j, b.t0);

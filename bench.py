@@ -63,17 +63,24 @@ def algorithmic_work(s: synth.Shape):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
-# ncu captures of the kernels, taken at T = TRAFFIC["T"] tokens and scaled to
-# the workload by its tokens.  Each figure describes the device code of its
+# ncu captures of the kernels (one kernel per capture), taken at T =
+# TRAFFIC["T"] tokens and scaled to the workload by its tokens (no scaling at
+# the training shape).  Each figure describes the device code of its
 # kernel as it was captured (the digest of the kernel's source file and the
 # shared device headers) and is reported as null for any other.
-KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu"}
+KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu", "quant": "quant.cu"}
 TRAFFIC = {
-    "T": 24576,
-    "sources_sha256": {"bwd": "dfe7c1bb9b32051e09ed8bdbd973db66ca4bc7b64f1a4121b77e13eee85e4a55", "gemm": "a8e5973c0c9b9c5d9224d1b25ad9cc5732e13f9b71f559a2c93cb10a9b329e91"},
-    # dw_gemm: the GEMM and its split-reduction kernel (one span)
-    "bytes": {"dy_amax": ("bwd", 158.45e6), "dy_quant": ("bwd", 179.94e6), "fwd_gemm": ("gemm", 64.50e6),
-              "dx_gemm": ("gemm", 52.67e6), "dw_gemm": ("gemm", 86.34e6)},
+    "T": 49152,
+    "sources_sha256": {"bwd": "2280a53cb62ce68a8852253d56e2721cd892151da48698f346922e9c783bd463",
+                       "gemm": "5ff61c193954e32ba3faa8fe5b8f5d1c30be446e22014f1dcb9e2db40522797c",
+                       "quant": "1e8c6fcd57f29fa5db06110ea2bc9f72aa8e7b431e6979f8bcadae321cafd08a"},
+    # mean of two launches of the full-size step; dw_gemm: the GEMM and its
+    # split-reduction kernel (one span); bank_refresh: the one-layer refresh
+    # of the step
+    "bytes": {"dy_amax": ("bwd", 3.093e+08), "dy_quant": ("bwd", 3.792e+08),
+              "fwd_gemm": ("gemm", 1.779e+08), "dx_gemm": ("gemm", 1.319e+08),
+              "dw_gemm": ("gemm", 1.515e+08), "x_quant": ("quant", 7.951e+07),
+              "bank_refresh": ("quant", 2.982e+06)},
 }
 
 
@@ -338,6 +345,8 @@ def run_ours(args, rank, world):
     peaks = load_peaks()
     fp8 = fp8_peak(peaks)
     kern = kernel_table(per, work, peaks)
+    for name in kern:                # DRAM bytes per launch from the ncu captures (null if not this build's)
+        kern[name]["traffic"] = traffic_for(name, s.T)
     dom = max(KERNELS, key=lambda k: per[k])
     bound, amount = work[dom]
     roofline = dict(kernel=dom, bound=bound, achieved=kern[dom]["achieved"],

@@ -497,7 +497,6 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
 
   const int T = dims->T, D = dims->D, H = dims->H, dqk = dims->d_qk, dvw = dims->d_v;
   const int N = H * (2 * dqk + dvw);
-  const int tiles = (T + 127) / 128;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* dyparts = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
@@ -505,12 +504,13 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   const DevStatus st = dev_status(ws);
 
   BwdMaps m;
-  bool ok = map3d(&m.dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dq, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map3d(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map3d(&m.dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map3d(&m.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, dvw, T, H, 32, 128, 1, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map2d(&m.dy8, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 32, 128, CU_TENSOR_MAP_SWIZZLE_32B);
+  constexpr uint32_t R = kBwdUnitRows;
+  bool ok = map3d(&m.dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dq, dqk, T, H, 32, R, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, R, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&m.dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dk, dqk, T, H, 32, R, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, R, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&m.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv, dvw, T, H, 32, R, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map2d(&m.dy8, CU_TENSOR_MAP_DATA_TYPE_UINT8, dY8, N, T, N, 32, R, CU_TENSOR_MAP_SWIZZLE_32B);
   if (!ok) return QKVP_ERR_CUDA;
 
   BwdParams bp;
@@ -519,8 +519,8 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   bp.d_qk = dqk;
   bp.d_v = dvw;
   bp.N = N;
-  bp.tiles = tiles;
-  bp.num_units = tiles * H * 3;
+  bp.tiles = (T + kBwdUnitRows - 1) / kBwdUnitRows;
+  bp.num_units = bp.tiles * H * 3;
   bp.rstd = rstd;
   bp.pos = pos;
   bp.rope = rope_table;

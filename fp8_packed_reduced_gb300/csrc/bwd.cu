@@ -12,11 +12,11 @@
 // (RoPE is a rotation, so the inner product needs no rotation and one
 // inverse rotation of (g_out - mu * o) suffices).  dY_v = dv.
 //
-// Work unit: 128 tokens x one head x one part (q, k or v); a group takes the
+// Work unit: 64 tokens x one head x one part (q, k or v); a group takes the
 // three parts of one (token tile, head) in a row, so that the k part reuses
-// the RoPE factors of the q part.  Persistent CTA per SM of two groups of
-// eight warps; each group owns its own ring of input stages, which one of its threads refills
-// by TMA (the unit's [128 tokens x 32 cols] boxes, 64-byte swizzle) as soon
+// the RoPE factors of the q part.  Persistent CTA per SM of four groups of
+// four warps; each group owns its own ring of input stages, which one of its threads refills
+// by TMA (the unit's [64 tokens x 32 cols] boxes, 64-byte swizzle) as soon
 // as the group has read a stage.  Two threads per token row: thread half h
 // owns the 8-column blocks (c / 8) % 2 == h of the row, which keeps each
 // rotation pair (i, i + d/2) in one thread; the row's mean(g_out * o) is one
@@ -36,20 +36,22 @@
 
 namespace qkvp {
 
-constexpr int kInBox = 8192;        // 128 rows x 32 bf16
-constexpr int kOutBox = 4096;       // 128 rows x 32 codes
-constexpr int kGroupThreads = 256;
-constexpr int kBwdThreads = 2 * kGroupThreads;
+constexpr int kRows = kBwdUnitRows;   // tokens per unit
+constexpr int kInBox = kRows * 64;    // kRows rows x 32 bf16
+constexpr int kOutBox = kRows * 32;   // kRows rows x 32 codes
+constexpr int kGroupThreads = 2 * kRows;   // two threads per token row
+constexpr int kGroups = 4;                 // consumer groups per CTA
+constexpr int kBwdThreads = kGroups * kGroupThreads;
 constexpr int kMaxStagesPerGroup = 3;
 
 __host__ __device__ constexpr int bwd_stage_bytes(int d_qk) {
   return (2 * d_qk > 128 ? 2 * d_qk : 128) / 32 * kInBox;   // max(dq+q, dv) boxes
 }
 // Input stages owned by each consumer group, as many as fit beside the code
-// staging: 3 at d_qk = 64 (32 KB stages), 2 at 96 (48 KB), 1 at 128 (64 KB).
+// staging: 3 at d_qk = 64 (16 KB stages), 2 at 96 (24 KB), 1 at 128 (32 KB).
 __host__ __device__ constexpr int bwd_stages_per_group(int d_qk) { return d_qk <= 64 ? 3 : d_qk <= 96 ? 2 : 1; }
 __host__ __device__ constexpr int bwd_smem_bytes(int d_qk, bool quant) {
-  return 1024 + 2 * bwd_stages_per_group(d_qk) * bwd_stage_bytes(d_qk) + (quant ? 2 * 4 * kOutBox : 0);
+  return 1024 + kGroups * bwd_stages_per_group(d_qk) * bwd_stage_bytes(d_qk) + (quant ? kGroups * 4 * kOutBox : 0);
 }
 
 struct BwdUnit {
@@ -60,7 +62,7 @@ __device__ __forceinline__ BwdUnit bwd_decode(const BwdParams& p, int u) {
   BwdUnit b;
   b.part = u % 3;
   b.h = (u / 3) % p.H;
-  b.t0 = (u / (3 * p.H)) * 128;
+  b.t0 = (u / (3 * p.H)) * kRows;
   b.col0 = b.part == 0 ? b.h * p.d_qk : b.part == 1 ? (p.H + b.h) * p.d_qk : 2 * p.H * p.d_qk + b.h * p.d_v;
   return b;
 }
@@ -99,7 +101,7 @@ __device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
 }
 
 // Eight codes of columns [c, c + 8) (c % 8 == 0) of row r into the
-// token-major staging boxes [128 rows][32 codes] with 32-byte swizzling
+// token-major staging boxes [64 rows][32 codes] with 32-byte swizzling
 // (the 16-byte half of a row is XORed with bit 2 of the row).
 __device__ __forceinline__ void emit8(const f2 (&v)[4], const Bracket2& k, int r, int c, uint8_t* out8) {
   const uint2 w = quant8(v, k);
@@ -143,13 +145,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int NG = HALF / 16;      // 16-pair groups; this thread owns 8 pairs of each
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[2 * kMaxStagesPerGroup];
+  __shared__ __align__(8) uint64_t full[kGroups * kMaxStagesPerGroup];
   // per group and stage: every thread of the group is done with the stage's
   // current unit (and, in pass 2, has staged its codes); the group's thread 0
   // waits on it alone.  One barrier per stage: a thread that runs ahead can
   // only arrive again on a stage after thread 0 has refilled it, which it
   // does once the earlier phase has completed.
-  __shared__ __align__(8) uint64_t done[2][kMaxStagesPerGroup];
+  __shared__ __align__(8) uint64_t done[kGroups][kMaxStagesPerGroup];
   __shared__ float red[32];
   __shared__ int abort_flag;
   const int g = threadIdx.x / kGroupThreads;    // consumer group
@@ -159,8 +161,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < 2 * SPG; ++s) mbar_init(&full[s], 1);
-    for (int gg = 0; gg < 2; ++gg)
+    for (int s = 0; s < kGroups * SPG; ++s) mbar_init(&full[s], 1);
+    for (int gg = 0; gg < kGroups; ++gg)
       for (int s = 0; s < SPG; ++s) mbar_init(&done[gg][s], kGroupThreads);
     fence_mbar_init();
   }
@@ -174,9 +176,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   uint8_t* stages = smem + g * SPG * kStage;                 // this group's input stages
-  uint8_t* out8 = smem + 2 * SPG * kStage + g * 4 * kOutBox;  // and its code staging
+  uint8_t* out8 = smem + kGroups * SPG * kStage + g * 4 * kOutBox;  // and its code staging
   uint64_t* gfull = full + g * SPG;
-  const int ustep = 2 * gridDim.x;
+  const int ustep = kGroups * gridDim.x;
   // Input loads of unit u into stage s (thread gt == 0 only).  `inflight`
   // and `inpar` record the stages whose loads have not been waited for.
   uint32_t inflight = 0, inpar = 0;

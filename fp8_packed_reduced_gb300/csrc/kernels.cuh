@@ -152,9 +152,11 @@ struct BwdParams {
   int nparts;            // grid of pass 1
   float* dy_scale;       // written by pass 2
 };
+// Tokens per work unit of the backward epilogue (the height of its TMA boxes).
+constexpr int kBwdUnitRows = 64;
 struct BwdMaps {
-  CUtensorMap dq, q, dk, k, dv;   // loads, 3-D [H][T][d], box {32, 128, 1}, 64-byte swizzle
-  CUtensorMap dy8;                // store: [T][N] codes, box {32, 128}, 32-byte swizzle
+  CUtensorMap dq, q, dk, k, dv;   // loads, 3-D [H][T][d], box {32, kBwdUnitRows, 1}, 64-byte swizzle
+  CUtensorMap dy8;                // store: [T][N] codes, box {32, kBwdUnitRows}, 32-byte swizzle
 };
 cudaError_t launch_bwd_amax(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s);
 cudaError_t launch_bwd_quant(const BwdMaps& m, const BwdParams& p, int grid, DevStatus st, cudaStream_t s);

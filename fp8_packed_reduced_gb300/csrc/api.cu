@@ -394,9 +394,9 @@ int forward_gemm(const qkvp_dims* dims, float eps, const float* rope_table, int 
   ok = ok && map2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, hq * dqk / pair,
                    CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && map2d(&tm_wv, CU_TENSOR_MAP_DATA_TYPE_UINT8, W8, D, N, D, 128, 2 * dv / pair, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && map3d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 32, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && map3d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dqk, T, H, 64, 32, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dqk, T, H, 64, 32, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && map3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dv, T, H, 64, 32, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return QKVP_ERR_CUDA;
   FwdParams p;
   p.T = T;

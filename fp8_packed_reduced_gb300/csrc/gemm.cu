@@ -288,6 +288,16 @@ __device__ __forceinline__ void stage_chunk_sw64(uint8_t* box, int row, int col_
 }
 
 // Stage 16 consecutive bf16 columns [c0, c0+16) of one row (c0 % 16 == 0)
+// into consecutive boxes of 32 rows x 64 columns (128 B rows, 128-byte
+// swizzling: the 16-byte chunk index is XORed with the row's low three bits).
+__device__ __forceinline__ void stage16_sw128(uint8_t* boxes, int row, int c0, const uint32_t (&w)[8]) {
+  uint8_t* box = boxes + (c0 >> 6) * 4096 + row * 128;
+  const int cc = (c0 & 63) >> 3;
+  *reinterpret_cast<uint4*>(box + ((cc ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(box + (((cc + 1) ^ (row & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Stage 16 consecutive bf16 columns [c0, c0+16) of one row (c0 % 16 == 0)
 // into a group of consecutive 2 KB boxes.
 __device__ __forceinline__ void stage16(uint8_t* boxes, int row, int c0, const uint32_t (&w)[8]) {
   uint8_t* box = boxes + (c0 >> 5) * 2048;
@@ -369,7 +379,7 @@ struct FwdEpi {
   const CUtensorMap* tk;
   const CUtensorMap* tv;
   const DevStatus& st;
-  uint8_t* stage;   // 8 KB: one head's boxes
+  uint8_t* stage;   // 8 KB: one head's boxes (32 rows x 64 columns each)
   int qw, sub, nsub, lane;
   float sxw;
   // per unit, set by prepare() before the accumulator is ready: tile decode,
@@ -462,15 +472,17 @@ struct FwdEpi {
             lo[w] = f2_to_bf16x2(f2_sub(f2_mul(a, c), f2_mul(b, sn)));   // a cos - b sin
             hi[w] = f2_to_bf16x2(f2_fma(a, sn, f2_mul(b, c)));           // b cos + a sin
           }
-          stage16(buf, lane, g * 16, lo);
-          stage16(buf, lane, HALF + g * 16, hi);
+          stage16_sw128(buf, lane, g * 16, lo);
+          stage16_sw128(buf, lane, HALF + g * 16, hi);
         }
         fence_async_smem();
         __syncwarp();
         if (lane == 0 && ty < p.T) {   // (a pair's second tile may lie wholly past T)
           const CUtensorMap* map = kind == 0 ? tq : tk;
 #pragma unroll
-          for (int b = 0; b < DQK / 32; ++b) tma_store_3d(map, buf + b * 2048, 32 * b, ty, h);
+          // 64-column boxes (the columns of a second box past d_qk = 96 lie
+          // outside the tensor and are not written)
+          for (int b = 0; b < (DQK + 63) / 64; ++b) tma_store_3d(map, buf + b * 4096, 64 * b, ty, h);
           bulk_commit();
         }
       } else {
@@ -489,14 +501,14 @@ struct FwdEpi {
             for (int i = 0; i < 8; ++i)
               w[i] = f2_to_bf16x2(
                   f2_mul(f2_make(__uint_as_float(raw[g * 16 + 2 * i]), __uint_as_float(raw[g * 16 + 2 * i + 1])), sc));
-            stage16(buf, lane, hf * 64 + g * 16, w);
+            stage16_sw128(buf, lane, hf * 64 + g * 16, w);
           }
         }
         fence_async_smem();
         __syncwarp();
         if (lane == 0 && ty < p.T) {
 #pragma unroll
-          for (int b = 0; b < 4; ++b) tma_store_3d(tv, buf + b * 2048, 32 * b, ty, h);
+          for (int b = 0; b < 2; ++b) tma_store_3d(tv, buf + b * 4096, 64 * b, ty, h);
           bulk_commit();
         }
       }

@@ -71,16 +71,16 @@ def algorithmic_work(s: synth.Shape):
 KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu", "quant": "quant.cu"}
 TRAFFIC = {
     "T": 49152,
-    "sources_sha256": {"bwd": "2280a53cb62ce68a8852253d56e2721cd892151da48698f346922e9c783bd463",
-                       "gemm": "5ff61c193954e32ba3faa8fe5b8f5d1c30be446e22014f1dcb9e2db40522797c",
-                       "quant": "1e8c6fcd57f29fa5db06110ea2bc9f72aa8e7b431e6979f8bcadae321cafd08a"},
+    "sources_sha256": {"bwd": "6bc1f7bb3d1252e924378592d3f363d61cda1e888bbadd52a7677702a8c916e8",
+                       "gemm": "72482ff55592edbe32738b97439e95df574cc1c94b22f409232ee037281f92e3",
+                       "quant": "135a59af90f9cee77e348307d79a765717331b7445543ab6a5e5f899f9dfacec"},
     # mean of two launches of the full-size step; dw_gemm: the GEMM and its
     # split-reduction kernel (one span); bank_refresh: the one-layer refresh
     # of the step
-    "bytes": {"dy_amax": ("bwd", 3.093e+08), "dy_quant": ("bwd", 3.792e+08),
-              "fwd_gemm": ("gemm", 1.779e+08), "dx_gemm": ("gemm", 1.319e+08),
-              "dw_gemm": ("gemm", 1.515e+08), "x_quant": ("quant", 7.951e+07),
-              "bank_refresh": ("quant", 2.982e+06)},
+    "bytes": {"dy_amax": ("bwd", 3.092e+08), "dy_quant": ("bwd", 3.789e+08),
+              "fwd_gemm": ("gemm", 1.753e+08), "dx_gemm": ("gemm", 1.334e+08),
+              "dw_gemm": ("gemm", 1.515e+08), "x_quant": ("quant", 7.954e+07),
+              "bank_refresh": ("quant", 2.98e+06)},
 }
 
 

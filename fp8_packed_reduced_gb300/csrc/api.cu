@@ -377,6 +377,26 @@ int qkvp_quantize_bank(int L, int D, int H, int d_qk, int d_v, const uint16_t* c
 namespace {
 // The packed GEMM with its fused epilogue, from x8 and its scale (arguments
 // already validated).
+// Slots of a token block in the order q, v, k tiles are interleaved in
+// proportion to their counts: tile i of a list of n sits at (2i + 1) / 2n,
+// ties in the order q, v, k (nq = nv = 3 gives q0 v0 k0 q1 v1 k1 q2 v2 k2).
+static void fwd_tile_order(FwdParams& p) {
+  const int first[3] = {0, 2 * p.nq, p.nq};   // q, v, k tiles
+  const int count[3] = {p.nq, p.nv, p.nq};
+  int next[3] = {0, 0, 0};
+  for (int slot = 0; slot < p.n_tiles; ++slot) {
+    int best = -1;
+    for (int l = 0; l < 3; ++l) {
+      if (next[l] >= count[l]) continue;
+      // compare (2 next[l] + 1) / count[l] across lists without division
+      if (best < 0 || static_cast<int64_t>(2 * next[l] + 1) * count[best] <
+                          static_cast<int64_t>(2 * next[best] + 1) * count[l])
+        best = l;
+    }
+    p.tile_order[slot] = static_cast<uint8_t>(first[best] + next[best]++);
+  }
+}
+
 int forward_gemm(const qkvp_dims* dims, float eps, const float* rope_table, int max_pos, const uint8_t* x8,
                  const float* x_scale, const int32_t* pos, const uint8_t* W8, const float* w_scale, uint16_t* q,
                  uint16_t* k, uint16_t* v, float* rstd, void* ws, int sms, cudaStream_t s) {
@@ -407,6 +427,7 @@ int forward_gemm(const qkvp_dims* dims, float eps, const float* rope_table, int 
   p.nq = (H + p.hq - 1) / p.hq;
   p.nv = (H + 1) / 2;
   p.n_tiles = 2 * p.nq + p.nv;
+  fwd_tile_order(p);
   p.pair = pair;
   p.num_units = (tiles + pair - 1) / pair * p.n_tiles;
   p.kblocks = D / 128;

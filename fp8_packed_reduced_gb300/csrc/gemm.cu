@@ -326,6 +326,8 @@ struct FwdSched {
     tma_load_2d_at<PAIR>(sB, ui.b_sel == 0 ? b : tmBv, bar, kb * kBK, ui.b_row);
   }
   __device__ int num_units() const { return p.num_units; }
+  // tile (index into q tiles, then k tiles, then v tiles) of unit u
+  __device__ int tile(int u) const { return p.tile_order[u % p.n_tiles]; }
   // kind 0 = q, 1 = k, 2 = v
   __device__ void decode(int j, int& kind, int& head0, int& nh) const {
     if (j < p.nq) {
@@ -343,7 +345,7 @@ struct FwdSched {
     }
   }
   __device__ Unit unit(int u) const {
-    const int j = u % p.n_tiles;
+    const int j = tile(u);
     int kind, head0, nh;
     decode(j, kind, head0, nh);
     Unit r;
@@ -379,7 +381,7 @@ struct FwdEpi {
   const CUtensorMap* tk;
   const CUtensorMap* tv;
   const DevStatus& st;
-  uint8_t* stage;   // 8 KB: one head's boxes (32 rows x 64 columns each)
+  uint8_t* stage;   // 4 KB: one box of 32 rows x 64 columns
   int qw, sub, nsub, lane;
   float sxw;
   // per unit, set by prepare() before the accumulator is ready: tile decode,
@@ -391,7 +393,7 @@ struct FwdEpi {
   __device__ void post(int) {}
   __device__ void prepare(int u) {
     const int m = sc.mtile(u);
-    sc.decode(u % p.n_tiles, kind, head0, nh);
+    sc.decode(sc.tile(u), kind, head0, nh);
     t = m * kBM + qw * 32 + lane;
     valid = t < p.T;
     int pos = 0;
@@ -417,21 +419,34 @@ struct FwdEpi {
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
   }
-  // wait until the previous head's store has read the staging boxes
+  // wait until the previous store has read the staging box
   __device__ uint8_t* acquire() {
     if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
     return stage;
   }
+  // the staged box goes to columns [x0, x0 + 64) of head h, rows ty..ty+31
+  __device__ void store_box(const CUtensorMap* map, int x0, int ty, int h) {
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0 && ty < p.T) {   // (a pair's second tile may lie wholly past T)
+      tma_store_3d(map, stage, x0, ty, h);
+      bulk_commit();
+    }
+  }
 
+  // One head's output leaves in 64-column boxes through the warp's single
+  // staging box: columns [0, 64) first, then (d > 64) columns [64, d), the
+  // columns of that box past d lying outside the tensor and not written.
   template <class Release>
   __device__ void process(int u, uint32_t tacc, Release& release) {
     constexpr int HALF = DQK / 2;
+    constexpr int NG = HALF / 16;                           // rotation groups of 16 pairs
+    constexpr int G1 = HALF >= 64 ? 0 : (64 - HALF) / 16;   // groups whose upper columns lie in box 0
     const int ty = sc.mtile(u) * kBM + qw * 32;
     for (int hh = sub; hh < nh; hh += nsub) {  // this warp's heads of the unit
       const int h = head0 + hh;
       const bool last_head = hh + nsub >= nh;
-      uint8_t* buf = acquire();
       if (kind < 2) {
         // pass 1: sum of squares of the raw accumulators (scaled once below)
         f2 ss2 = 0;
@@ -452,9 +467,13 @@ struct FwdEpi {
         const float r = 1.0f / sqrtf(__fdiv_rn(ss, static_cast<float>(DQK)) + p.eps);
         if (valid) p.rstd[(static_cast<int64_t>(kind) * p.H + h) * p.T + t] = r;
         const f2 f = f2_make(sxw * r, sxw * r);   // accumulator -> normalised value
-        // pass 2: rotate 16 pairs at a time, columns [16g, 16g+16) and [HALF+16g, HALF+16g+16)
+        // pass 2: rotate 16 pairs at a time, columns [16g, 16g+16) and
+        // [HALF+16g, HALF+16g+16); upper columns at or past 64 wait in
+        // registers until box 0 has left
+        uint32_t keep[NG - G1 > 0 ? NG - G1 : 1][8];
+        uint8_t* buf = acquire();
 #pragma unroll
-        for (int g = 0; g < HALF / 16; ++g) {
+        for (int g = 0; g < NG; ++g) {
           float4 cs[8];
 #pragma unroll
           for (int w = 0; w < 8; ++w) cs[w] = __ldg(rope_row + static_cast<int64_t>(g * 8 + w) * p.max_pos);
@@ -462,7 +481,7 @@ struct FwdEpi {
           tmem_ld16(tacc + hh * DQK + g * 16, ra);
           tmem_ld16(tacc + hh * DQK + HALF + g * 16, rb);
           tmem_ld_wait();
-          if (last_head && g == HALF / 16 - 1) release();
+          if (last_head && g == NG - 1) release();
           uint32_t lo[8], hi[8];
 #pragma unroll
           for (int w = 0; w < 8; ++w) {
@@ -473,17 +492,20 @@ struct FwdEpi {
             hi[w] = f2_to_bf16x2(f2_fma(a, sn, f2_mul(b, c)));           // b cos + a sin
           }
           stage16_sw128(buf, lane, g * 16, lo);
-          stage16_sw128(buf, lane, HALF + g * 16, hi);
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0 && ty < p.T) {   // (a pair's second tile may lie wholly past T)
-          const CUtensorMap* map = kind == 0 ? tq : tk;
+          if (g < G1) {
+            stage16_sw128(buf, lane, HALF + g * 16, hi);
+          } else {
 #pragma unroll
-          // 64-column boxes (the columns of a second box past d_qk = 96 lie
-          // outside the tensor and are not written)
-          for (int b = 0; b < (DQK + 63) / 64; ++b) tma_store_3d(map, buf + b * 4096, 64 * b, ty, h);
-          bulk_commit();
+            for (int w = 0; w < 8; ++w) keep[g - G1][w] = hi[w];
+          }
+        }
+        const CUtensorMap* map = kind == 0 ? tq : tk;
+        store_box(map, 0, ty, h);
+        if (DQK > 64) {
+          buf = acquire();
+#pragma unroll
+          for (int g = G1; g < NG; ++g) stage16_sw128(buf, lane, HALF + g * 16 - 64, keep[g - G1]);
+          store_box(map, 64, ty, h);
         }
       } else {
 #pragma unroll
@@ -494,6 +516,7 @@ struct FwdEpi {
           tmem_ld_wait();
           if (last_head && hf == 1) release();
           const f2 sc = f2_make(sxw, sxw);
+          uint8_t* buf = acquire();
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint32_t w[8];
@@ -501,15 +524,9 @@ struct FwdEpi {
             for (int i = 0; i < 8; ++i)
               w[i] = f2_to_bf16x2(
                   f2_mul(f2_make(__uint_as_float(raw[g * 16 + 2 * i]), __uint_as_float(raw[g * 16 + 2 * i + 1])), sc));
-            stage16_sw128(buf, lane, hf * 64 + g * 16, w);
+            stage16_sw128(buf, lane, g * 16, w);
           }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0 && ty < p.T) {
-#pragma unroll
-          for (int b = 0; b < 2; ++b) tma_store_3d(tv, buf + b * 4096, 64 * b, ty, h);
-          bulk_commit();
+          store_box(tv, 64 * hf, ty, h);
         }
       }
     }
@@ -518,7 +535,7 @@ struct FwdEpi {
 
 // Epilogue warps and per-warp staging bytes of each GEMM.
 constexpr int kFwdEW = 8, kDwEW = kDwEpiWarps;
-constexpr int kFwdEPB = 8192, kDxEPB = 8192;
+constexpr int kFwdEPB = 4096, kDxEPB = 8192;
 
 template <int DQK, bool PAIR>
 __global__ void __launch_bounds__(gemm_threads(kFwdEW), 1)

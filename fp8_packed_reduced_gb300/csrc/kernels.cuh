@@ -72,12 +72,17 @@ cudaError_t launch_selftest_wait(DevStatus st, cudaStream_t s);
 // tile computed by a 2-CTA cluster (one MMA per K step over both CTAs'
 // shared memory); with pair = 1 a 128-row tile computed by one CTA.
 // ---------------------------------------------------------------------------
+constexpr int kMaxFwdTiles = 192;   // 2 * 64 q/k tiles + 64 v tiles at H = 128
 struct FwdParams {
   int T, H, d_qk, d_v;
   int hq;            // heads per Q (or K) tile
   int nq;            // Q tiles (= K tiles) per 128-token block
   int nv;            // V tiles per block (2 heads each)
   int n_tiles;       // 2*nq + nv
+  // tile of each slot of a token block: q, v and k tiles interleaved in
+  // proportion, so that a CTA's consecutive units alternate between the
+  // q/k epilogue (norm and rotation) and the lighter v one
+  uint8_t tile_order[kMaxFwdTiles];
   int pair;          // CTAs per unit (1 or 2)
   int num_units;     // ceil(ceil(T/128) / pair) * n_tiles
   int kblocks;       // D / 128

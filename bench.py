@@ -71,15 +71,15 @@ def algorithmic_work(s: synth.Shape):
 KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu", "quant": "quant.cu"}
 TRAFFIC = {
     "T": 49152,
-    "sources_sha256": {"bwd": "6bc1f7bb3d1252e924378592d3f363d61cda1e888bbadd52a7677702a8c916e8",
-                       "gemm": "72482ff55592edbe32738b97439e95df574cc1c94b22f409232ee037281f92e3",
-                       "quant": "135a59af90f9cee77e348307d79a765717331b7445543ab6a5e5f899f9dfacec"},
+    "sources_sha256": {"bwd": "bdb1d24aa9a5afde32177ee9f1d8a3442c8ba6df5429fd212a10394977bbe770",
+                       "gemm": "0bcdc838839202ac020f87d9b9e6e03df884b5631087567f514316c2050e7717",
+                       "quant": "eecda256b77c1961fbabaade87d331b0efed39bd68636feefa33ae38608055ca"},
     # mean of two launches of the full-size step; dw_gemm: the GEMM and its
     # split-reduction kernel (one span); bank_refresh: the one-layer refresh
     # of the step
-    "bytes": {"dy_amax": ("bwd", 3.092e+08), "dy_quant": ("bwd", 3.789e+08),
-              "fwd_gemm": ("gemm", 1.753e+08), "dx_gemm": ("gemm", 1.334e+08),
-              "dw_gemm": ("gemm", 1.515e+08), "x_quant": ("quant", 7.954e+07),
+    "bytes": {"dy_amax": ("bwd", 3.092e+08), "dy_quant": ("bwd", 3.787e+08),
+              "fwd_gemm": ("gemm", 1.751e+08), "dx_gemm": ("gemm", 1.319e+08),
+              "dw_gemm": ("gemm", 1.514e+08), "x_quant": ("quant", 7.954e+07),
               "bank_refresh": ("quant", 2.98e+06)},
 }
 

@@ -263,6 +263,37 @@ def test_backward_deterministic(qk):
         assert torch.equal(a[name], b[name]), name
 
 
+def _step_outputs(qk, inp, g, W8, W8T, w_scale, table, ws, H):
+    q, k, v, saved = qk.forward(inp["x"], inp["pos"], W8, w_scale, H, table, ws=ws)
+    out = qk.backward(g["dq"], g["dk"], g["dv"], saved, W8T, w_scale, table, ws=ws)
+    return dict(q=q, k=k, v=v, rstd=saved.rstd, x8=saved.x8, dY8=out["dY8"], dx=out["dx"], dW=out["dW"])
+
+
+def test_captured_step_replays_the_same_results(qk):
+    """Forward + backward replayed from a captured CUDA graph (as the bench
+    times it) give the bits of the same calls made eagerly."""
+    s = synth.Shape(T=1000, D=768, H=6, seq_len=1000)
+    inp = {n: t.to(DEV) for n, t in synth.forward_inputs(s, seed=7).items()}
+    g = {n: t.to(DEV) for n, t in synth.backward_inputs(s, seed=7).items()}
+    W8, W8T, w_scale = qk.quantize_bank([(inp["Wq"], inp["Wk"], inp["Wv"])], s.H)
+    table = qk.build_rope_table(8192, s.d_qk, 10000.0, DEV)
+    ws = qk.new_workspace(qk.Shape(s.T, s.D, s.H), DEV)
+    args = (inp, g, W8[0], W8T[0], w_scale[0:1], table, ws, s.H)
+    eager = _step_outputs(qk, *args)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        _step_outputs(qk, *args)   # warm-up outside the capture
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            captured = _step_outputs(qk, *args)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert qk.poll_device_status(ws) == (qk.OK, 0)
+    for name, t in eager.items():
+        assert torch.equal(t, captured[name]), name
+
+
 # ----------------------------------------------------------------------------
 # Device-side error reporting (no fault, no hang)
 # ----------------------------------------------------------------------------

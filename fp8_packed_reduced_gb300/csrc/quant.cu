@@ -377,31 +377,34 @@ __device__ __forceinline__ void grid_barrier(GridBar* bar, const DevStatus& st, 
 }
 
 constexpr int kFusedThreads = 512;
+// Two blocks per SM at no more than 48 registers a thread, so that a quarter
+// of the register file stays free for another kernel's block beside them
+// (the bank refresh of the same step: 256 threads x 64 registers).
+constexpr int kFusedBlocksPerSm = 2;
+constexpr int kFusedMaxRegs = 48;
 
-__global__ void __launch_bounds__(kFusedThreads) x_amax_quant_kernel(const uint16_t* __restrict__ x, int64_t n16,
+__global__ void __maxnreg__(kFusedMaxRegs) x_amax_quant_kernel(const uint16_t* __restrict__ x, int64_t n16,
                                                                      uint8_t* __restrict__ x8, float* partials,
                                                                      float* x_scale, GridBar* bar, DevStatus st) {
   __shared__ float red[32];
   const uint4* src = reinterpret_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  // 1: amax over this block's groups of 16 values (four groups in flight);
-  // the lines are kept in L2 with priority for step 2
-  const uint64_t keep = l2_policy_evict_last();
+  // 1: amax over this block's groups of 16 values (four groups in flight)
   float m = 0.f;
   int64_t i = i0;
   for (; i + 3 * stride < n16; i += 4 * stride) {
     uint4 v[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      v[2 * j] = ldg_hint(src + 2 * (i + j * stride), keep);
-      v[2 * j + 1] = ldg_hint(src + 2 * (i + j * stride) + 1, keep);
+      v[2 * j] = __ldg(src + 2 * (i + j * stride));
+      v[2 * j + 1] = __ldg(src + 2 * (i + j * stride) + 1);
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) m = fmaxf(m, absmax_bf16x8(v[j]));
   }
   for (; i < n16; i += stride)
-    m = fmaxf(m, fmaxf(absmax_bf16x8(ldg_hint(src + 2 * i, keep)), absmax_bf16x8(ldg_hint(src + 2 * i + 1, keep))));
+    m = fmaxf(m, fmaxf(absmax_bf16x8(__ldg(src + 2 * i)), absmax_bf16x8(__ldg(src + 2 * i + 1))));
   m = block_max(m, red);
   if (threadIdx.x == 0) partials[blockIdx.x] = m;
   grid_barrier(bar, st, KID_X_QUANT);
@@ -442,6 +445,7 @@ cudaError_t launch_x_amax_quant(const uint16_t* x, int64_t n, uint8_t* x8, float
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, x_amax_quant_kernel, kFusedThreads, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (per_sm > kFusedBlocksPerSm) per_sm = kFusedBlocksPerSm;
     blocks = sms * per_sm < kMaxFusedBlocks ? sms * per_sm : kMaxFusedBlocks;
     if (dev < 64) cache[dev].store(blocks, std::memory_order_relaxed);
   }

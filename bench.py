@@ -73,13 +73,13 @@ TRAFFIC = {
     "T": 49152,
     "sources_sha256": {"bwd": "bdb1d24aa9a5afde32177ee9f1d8a3442c8ba6df5429fd212a10394977bbe770",
                        "gemm": "0bcdc838839202ac020f87d9b9e6e03df884b5631087567f514316c2050e7717",
-                       "quant": "eecda256b77c1961fbabaade87d331b0efed39bd68636feefa33ae38608055ca"},
+                       "quant": "fb6df8a58272a40bafb08c6a0c4901c1219b6a7b182c0084e35323529cb6d06a"},
     # mean of two launches of the full-size step; dw_gemm: the GEMM and its
     # split-reduction kernel (one span); bank_refresh: the one-layer refresh
     # of the step
     "bytes": {"dy_amax": ("bwd", 3.092e+08), "dy_quant": ("bwd", 3.787e+08),
               "fwd_gemm": ("gemm", 1.751e+08), "dx_gemm": ("gemm", 1.319e+08),
-              "dw_gemm": ("gemm", 1.514e+08), "x_quant": ("quant", 7.954e+07),
+              "dw_gemm": ("gemm", 1.514e+08), "x_quant": ("quant", 7.915e+07),
               "bank_refresh": ("quant", 2.98e+06)},
 }
 

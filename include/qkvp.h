@@ -197,9 +197,11 @@ int qkvp_forward(const qkvp_dims* dims, float eps,
  *            workspace of a forward/backward (its start serves); zeroed
  *            once with qkvp_workspace_init.  Calls sharing it must not
  *            overlap on the GPU.
- * The launch is persistent and its blocks meet at a grid-wide barrier, so all
- * of them must be resident at once: it may share the GPU with small kernels
- * of other streams, but two of these quantisations (this call, or the one
+ * The launch is persistent (two 512-thread blocks per SM, at most 48
+ * registers a thread, which leaves a quarter of each SM's registers to other
+ * kernels) and its blocks meet at a grid-wide barrier, so all of them must be
+ * resident at once: it may share the GPU with small kernels of other streams
+ * (the bank refresh, for one), but two of these quantisations (this call, or the one
  * inside qkvp_forward / qkvp_oproj_* / qkvp_mlp_*) running concurrently on
  * different streams, or a long persistent kernel holding the SMs, can keep
  * blocks out until the wait limit (qkvp_set_wait_timeout_ns) expires; the

@@ -72,7 +72,7 @@ KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu", "quant": "quant.cu"}
 TRAFFIC = {
     "T": 49152,
     "sources_sha256": {"bwd": "bdb1d24aa9a5afde32177ee9f1d8a3442c8ba6df5429fd212a10394977bbe770",
-                       "gemm": "0bcdc838839202ac020f87d9b9e6e03df884b5631087567f514316c2050e7717",
+                       "gemm": "e371ebde2dd6e58d9224daba4250adcfe01992e7d8c71252be43b99aef3284fe",
                        "quant": "fb6df8a58272a40bafb08c6a0c4901c1219b6a7b182c0084e35323529cb6d06a"},
     # mean of two launches of the full-size step; dw_gemm: the GEMM and its
     # split-reduction kernel (one span); bank_refresh: the one-layer refresh

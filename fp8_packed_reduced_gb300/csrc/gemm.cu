@@ -9,20 +9,21 @@
 //
 // One persistent, warp-specialised kernel body serves all three:
 //   warp 0     TMA producer: A tile (128 rows x 128 B of K) and B tile
-//              (ncols rows, loaded as 32-row boxes), 128-byte swizzle
+//              (one box of the tile's rows), 128-byte swizzle
 //   warp 1     TMEM allocator and MMA issuer (one thread): 4 MMAs of K = 32
 //              per stage, commit to the stage's "empty" barrier, and to the
 //              accumulator's "full" barrier after the last stage of a unit
-//   warps 2-9  epilogue, two warps per TMEM lane quarter (each owning half of
-//              the unit's heads or columns), one accumulator row (token) per
-//              thread; TMEM holds two 256-column accumulators so the
-//              epilogue of one unit overlaps the MMAs of the next
+//   warps 2-   epilogue, four or eight warps (one or two per TMEM lane
+//              quarter, each owning a share of the unit's heads or columns),
+//              one accumulator row (token) per thread; TMEM holds two
+//              256-column accumulators so the epilogue of one unit overlaps
+//              the MMAs of the next
 // On CTA pairs (a 2-CTA cluster, cta_group::2) a unit is a 256-row tile:
 // each CTA loads its own 128 rows of A and half of B (both halves complete
 // on the even CTA's stage barrier), the even CTA's MMA thread issues M = 256
 // MMAs over both CTAs' shared memory, each CTA's epilogue reads its own TMEM
 // rows, and the MMA commits arrive on both CTAs' barriers.  Per SM this halves
-// the shared-memory traffic of B (written by TMA, read by the MMA).
+// the bytes of B that TMA loads and writes into shared memory.
 // Every wait is bounded (see mbar_wait); on expiry the kernel records
 // QKVP_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <atomic>
@@ -66,7 +67,7 @@ struct Ring {
 };
 
 // Dynamic shared memory: alignment slack, the stage ring, and `epb` bytes of
-// output staging per epilogue warp (boxes of 32 rows x 64 B).
+// output staging per epilogue warp (boxes of 32 rows).
 __host__ __device__ constexpr int gemm_smem_bytes(Ring r, int ew, int epb) {
   return 1024 + r.stages * (kAStage + r.bstage) + ew * epb;
 }

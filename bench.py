@@ -671,19 +671,26 @@ def run_e2e(st: Step, args, dev, world):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s_in)
-    for i in range(steps):
-        one(i)
-    b.record(s_out)
-    torch.cuda.synchronize()
+    # three timed runs of `steps` steps each; the median run is reported (the
+    # host link is shared with the machine's other GPUs, and single runs have
+    # varied by up to 60 %)
+    runs = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_in)
+        for i in range(steps):
+            one(i)
+        b.record(s_out)
+        torch.cuda.synchronize()
+        runs.append(a.elapsed_time(b) / steps)
     for b_ in sets:
         code, where = qk.poll_device_status(b_.ws)
         if code != 0:
             raise RuntimeError(f"device status {qk.STATUS.get(code)} from kernel {where}")
-    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+    ms = max_over_ranks(sorted(runs)[1], world, dev)
     return {"value": round(job_tokens_per_s(st.s.T, world, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
-            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "runs_ms_per_step": [round(r, 4) for r in runs], "reported": "median of the three runs",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "overlap": "uploads, compute and downloads of neighbouring steps on three streams"}
 
 

@@ -97,8 +97,20 @@ def _compile(src: str, extra, verbose: bool) -> str:
 
 
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every unit under csrc/ and link libqkvp.so; returns its path."""
+    """Compile every unit under csrc/ and link libqkvp.so; returns its path.
+    Processes that build at once (the ranks of one job) take turns on a lock
+    file: the first compiles, the others find the stamps current."""
     os.makedirs(BUILD, exist_ok=True)
+    import fcntl
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(verbose, ptxas_info)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool, ptxas_info: bool) -> str:
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:

@@ -97,6 +97,7 @@ int qkvp::check_dims(const qkvp_dims* d) {
 namespace {
 
 // Workspace: [status 256 B][x amax partials][dY amax partials][dW partials]
+// (and, for the packed projection, [dY row means])
 constexpr size_t kStatusBytes = 256;
 constexpr int kMaxParts = 4096;
 constexpr size_t kPartsBytes = kMaxParts * sizeof(float);
@@ -119,7 +120,10 @@ size_t dw_partial_bytes(const DwShape& s, int splits) {
   return static_cast<size_t>(splits) * s.m_tiles * s.n_tiles * s.bn * 128 * sizeof(float);
 }
 size_t ws_bytes_for_shape(const DwShape& s) { return kStatusBytes + 2 * kPartsBytes + dw_partial_bytes(s, kMaxSplits); }
-size_t ws_bytes_for(const qkvp_dims* d) { return ws_bytes_for_shape(dw_shape(d)); }
+// The packed projection's workspace also holds the dY passes' row means
+// [2, H, T] float32 after the dW partials.
+size_t mu_bytes(const qkvp_dims* d) { return (static_cast<size_t>(2) * d->H * d->T * sizeof(float) + 15) / 16 * 16; }
+size_t ws_bytes_for(const qkvp_dims* d) { return ws_bytes_for_shape(dw_shape(d)) + mu_bytes(d); }
 
 // Split count for the dW GEMM: the fewest splits whose units fill the
 // workers (SMs, or SM pairs) in whole waves to >= 90%, with at least 4
@@ -522,6 +526,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* dyparts = reinterpret_cast<float*>(wsb + kStatusBytes + kPartsBytes);
   float* dwparts = reinterpret_cast<float*>(wsb + kStatusBytes + 2 * kPartsBytes);
+  float* mu = reinterpret_cast<float*>(wsb + ws_bytes_for_shape(dw_shape(dims)));
   const DevStatus st = dev_status(ws);
 
   BwdMaps m;
@@ -549,6 +554,7 @@ int qkvp_backward(const qkvp_dims* dims, const float* rope_table, int max_pos, c
   bp.partials = dyparts;
   bp.nparts = std::min({bp.num_units, sms, kMaxParts});
   bp.dy_scale = dy_scale;
+  bp.mu = mu;
   mark(s);
   QKVP_TRY_CUDA(launch_bwd_amax(m, bp, bp.nparts, st, s));
   mark(s);

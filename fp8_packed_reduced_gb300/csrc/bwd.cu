@@ -109,14 +109,20 @@ __device__ __forceinline__ void emit8(const f2 (&v)[4], const Bracket2& k, int r
   *reinterpret_cast<uint2*>(out8 + (c >> 5) * kOutBox + r * 32 + (((cl >> 4) ^ ((r >> 2) & 1)) << 4) + (cl & 15)) = w;
 }
 
-// Issue the loads of a q/k unit's per-row saved state: rstd and position
-// (0 for rows past T; the position is range-checked where it is used).
-__device__ __forceinline__ void row_state(const BwdParams& p, const BwdUnit& b, int t, float& rstd, int& pos) {
+// Issue the loads of a q/k unit's per-row saved state: rstd and position,
+// and in pass 2 the row's mean that pass 1 stored (0 for rows past T; the
+// position is range-checked where it is used).
+template <bool QUANT>
+__device__ __forceinline__ void row_state(const BwdParams& p, const BwdUnit& b, int t, float& rstd, int& pos,
+                                          float& mu) {
   rstd = 0.f;
   pos = 0;
+  mu = 0.f;
   if (t >= p.T) return;
-  rstd = __ldg(p.rstd + (static_cast<int64_t>(b.part) * p.H + b.h) * p.T + t);
+  const int64_t row = (static_cast<int64_t>(b.part) * p.H + b.h) * p.T + t;
+  rstd = __ldg(p.rstd + row);
   pos = __ldg(p.pos + t);
+  if (QUANT) mu = __ldg(p.mu + row);
 }
 
 // AND of `v` over the threads of consumer group g (all of them call it), so
@@ -233,11 +239,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float mx = 0.f;
   const float4* rope = reinterpret_cast<const float4*>(p.rope);
   // the saved state of the group's next q/k unit is loaded one unit ahead
-  float rstd_next = 0.f;
+  float rstd_next = 0.f, mu_next = 0.f;
   int pos_next = 0;
   if (unit_at(0) >= 0) {
     const BwdUnit b0 = bwd_decode(p, unit_at(0));
-    if (b0.part < 2) row_state(p, b0, b0.t0 + r, rstd_next, pos_next);
+    if (b0.part < 2) row_state<QUANT>(p, b0, b0.t0 + r, rstd_next, pos_next, mu_next);
   }
   // entry w of group gg: cos, cos, sin, sin of pairs c + 2w, c + 2w + 1
   float4 k4[NG][4];
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int s = k % SPG;
     const uint32_t par = (k / SPG) & 1;
     const BwdUnit b = bwd_decode(p, u);
-    const float rstd = rstd_next;
+    const float rstd = rstd_next, mu_row = mu_next;
     int pos = pos_next;
     // the q part's RoPE factors, in flight while the stage arrives and the
     // row's mean is formed (the k part that follows uses them again)
@@ -266,7 +272,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int un = unit_at(k + 1);
     if (un >= 0) {
       const BwdUnit bn = bwd_decode(p, un);
-      if (bn.part < 2) row_state(p, bn, bn.t0 + r, rstd_next, pos_next);
+      if (bn.part < 2) row_state<QUANT>(p, bn, bn.t0 + r, rstd_next, pos_next, mu_next);
     }
     if (QUANT) {
       // pass 2: thread 0 first lets the previous unit's codes leave the
@@ -284,18 +290,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int nbox;
     if (b.part < 2) {
       const uint8_t* in1 = in0 + (DQK / 32) * kInBox;
-      f2 acc = 0;
+      float mu = mu_row;   // pass 2: the mean pass 1 formed (the same arithmetic)
+      if (!QUANT) {
+        f2 acc = 0;
 #pragma unroll
-      for (int gg = 0; gg < NG; ++gg) {
-        const int c = 16 * gg + 8 * hf;
-        acc = dot8(load8(in0, r, c), load8(in1, r, c), acc);
-        acc = dot8(load8(in0, r, HALF + c), load8(in1, r, HALF + c), acc);
-        asm volatile("" ::: "memory");   // bounds the reads in flight (registers)
+        for (int gg = 0; gg < NG; ++gg) {
+          const int c = 16 * gg + 8 * hf;
+          acc = dot8(load8(in0, r, c), load8(in1, r, c), acc);
+          acc = dot8(load8(in0, r, HALF + c), load8(in1, r, HALF + c), acc);
+          asm volatile("" ::: "memory");   // bounds the reads in flight (registers)
+        }
+        const float2 a2 = f2_split(acc);
+        float dot = a2.x + a2.y;
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);   // the row's other half
+        mu = __fdiv_rn(dot, static_cast<float>(DQK));
+        // the means of four consecutive rows meet in lanes 0, 4, 16 and 20
+        // (rows 0-3, 4-7, 8-11, 12-15 of the warp) and leave as one 16-byte
+        // store where the row block is aligned and inside T
+        const float m1 = __shfl_down_sync(0xffffffffu, mu, 2);
+        const float m2 = __shfl_down_sync(0xffffffffu, mu, 8);
+        const float m3 = __shfl_down_sync(0xffffffffu, mu, 10);
+        if ((threadIdx.x & 11) == 0) {
+          const int t = b.t0 + r;
+          const int64_t at = (static_cast<int64_t>(b.part) * p.H + b.h) * p.T + t;
+          float* dst = p.mu + at;
+          if (t + 3 < p.T && (at & 3) == 0) {
+            *reinterpret_cast<float4*>(dst) = make_float4(mu, m1, m2, m3);
+          } else {
+            if (t < p.T) dst[0] = mu;
+            if (t + 1 < p.T) dst[1] = m1;
+            if (t + 2 < p.T) dst[2] = m2;
+            if (t + 3 < p.T) dst[3] = m3;
+          }
+        }
       }
-      const float2 a2 = f2_split(acc);
-      float dot = a2.x + a2.y;
-      dot += __shfl_xor_sync(0xffffffffu, dot, 1);   // the row's other half
-      const float mu = __fdiv_rn(dot, static_cast<float>(DQK));
       const f2 nmu = f2_make(-mu, -mu), rr = f2_make(rstd, rstd);
 #pragma unroll
       for (int gg = 0; gg < NG; ++gg) {

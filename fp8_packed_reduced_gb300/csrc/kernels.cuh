@@ -156,6 +156,7 @@ struct BwdParams {
   float* partials;       // amax partials (written by pass 1, read by pass 2)
   int nparts;            // grid of pass 1
   float* dy_scale;       // written by pass 2
+  float* mu;             // [2, H, T] mean(g_out * o) of every q/k row: pass 1 writes it, pass 2 reads it
 };
 // Tokens per work unit of the backward epilogue (the height of its TMA boxes).
 constexpr int kBwdUnitRows = 64;

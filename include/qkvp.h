@@ -78,8 +78,10 @@ const char* qkvp_status_string(int status);
  * barrier, which every call leaves ready for the next; zero it once with
  * qkvp_workspace_init before first use, and again after a device error (a
  * call that stopped early may leave the barrier mid-count).  It also holds
- * the amax partials and the dW GEMM's split partials.  Calls sharing one
- * workspace must not overlap on the GPU. */
+ * the amax partials, the dW GEMM's split partials and the backward's
+ * per-row means of the q/k gradients (2 * H * T floats, written by the dY amax
+ * pass and read by the quantise pass).  Calls sharing one workspace must not
+ * overlap on the GPU. */
 size_t qkvp_workspace_bytes(const qkvp_dims* dims);
 
 /* Bytes of scratch that qkvp_quantize_bank needs for L layers (0 if the

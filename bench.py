@@ -71,15 +71,15 @@ def algorithmic_work(s: synth.Shape):
 KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu", "quant": "quant.cu"}
 TRAFFIC = {
     "T": 49152,
-    "sources_sha256": {"bwd": "bdb1d24aa9a5afde32177ee9f1d8a3442c8ba6df5429fd212a10394977bbe770",
-                       "gemm": "e371ebde2dd6e58d9224daba4250adcfe01992e7d8c71252be43b99aef3284fe",
-                       "quant": "fb6df8a58272a40bafb08c6a0c4901c1219b6a7b182c0084e35323529cb6d06a"},
+    "sources_sha256": {"bwd": "87c21ed8d25857686e2eb57923f434afaf9a423fa09913950e692f8a5c4c1b0e",
+                       "gemm": "c9de075080dc23a9d5634eeef7ed9d35df6004e98cdbcb2d6a71d068e2d946c9",
+                       "quant": "270726eee5aada0c53740ecf87baf9304a5be421b85aac7ae31ba42d03c9339b"},
     # mean of two launches of the full-size step; dw_gemm: the GEMM and its
     # split-reduction kernel (one span); bank_refresh: the one-layer refresh
     # of the step
-    "bytes": {"dy_amax": ("bwd", 3.092e+08), "dy_quant": ("bwd", 3.787e+08),
-              "fwd_gemm": ("gemm", 1.751e+08), "dx_gemm": ("gemm", 1.319e+08),
-              "dw_gemm": ("gemm", 1.514e+08), "x_quant": ("quant", 7.915e+07),
+    "bytes": {"dy_amax": ("bwd", 3.099e+08), "dy_quant": ("bwd", 3.811e+08),
+              "fwd_gemm": ("gemm", 1.751e+08), "dx_gemm": ("gemm", 1.318e+08),
+              "dw_gemm": ("gemm", 1.515e+08), "x_quant": ("quant", 7.901e+07),
               "bank_refresh": ("quant", 2.98e+06)},
 }
 

@@ -140,6 +140,29 @@ __device__ __forceinline__ bool group_all(int g, bool v) {
   return out != 0;
 }
 
+// Pass 1 keeps each q/k row's mean for pass 2: the means of four
+// consecutive rows meet in lanes 0, 4, 16 and 20 (rows 0-3, 4-7, 8-11, 12-15
+// of the warp) and leave as one 16-byte store where the row block is aligned
+// and inside T.  Called by every lane of the warp.
+__device__ __forceinline__ void store_row_means(const BwdParams& p, const BwdUnit& b, int r, float mu) {
+  const float m1 = __shfl_down_sync(0xffffffffu, mu, 2);
+  const float m2 = __shfl_down_sync(0xffffffffu, mu, 8);
+  const float m3 = __shfl_down_sync(0xffffffffu, mu, 10);
+  if ((threadIdx.x & 11) == 0) {
+    const int t = b.t0 + r;
+    const int64_t at = (static_cast<int64_t>(b.part) * p.H + b.h) * p.T + t;
+    float* dst = p.mu + at;
+    if (t + 3 < p.T && (at & 3) == 0) {
+      *reinterpret_cast<float4*>(dst) = make_float4(mu, m1, m2, m3);
+    } else {
+      if (t < p.T) dst[0] = mu;
+      if (t + 1 < p.T) dst[1] = m1;
+      if (t + 2 < p.T) dst[2] = m2;
+      if (t + 3 < p.T) dst[3] = m3;
+    }
+  }
+}
+
 // One kernel body for both passes.  QUANT = false: amax partials; true: codes.
 template <int DQK, bool QUANT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -304,25 +327,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float dot = a2.x + a2.y;
         dot += __shfl_xor_sync(0xffffffffu, dot, 1);   // the row's other half
         mu = __fdiv_rn(dot, static_cast<float>(DQK));
-        // the means of four consecutive rows meet in lanes 0, 4, 16 and 20
-        // (rows 0-3, 4-7, 8-11, 12-15 of the warp) and leave as one 16-byte
-        // store where the row block is aligned and inside T
-        const float m1 = __shfl_down_sync(0xffffffffu, mu, 2);
-        const float m2 = __shfl_down_sync(0xffffffffu, mu, 8);
-        const float m3 = __shfl_down_sync(0xffffffffu, mu, 10);
-        if ((threadIdx.x & 11) == 0) {
-          const int t = b.t0 + r;
-          const int64_t at = (static_cast<int64_t>(b.part) * p.H + b.h) * p.T + t;
-          float* dst = p.mu + at;
-          if (t + 3 < p.T && (at & 3) == 0) {
-            *reinterpret_cast<float4*>(dst) = make_float4(mu, m1, m2, m3);
-          } else {
-            if (t < p.T) dst[0] = mu;
-            if (t + 1 < p.T) dst[1] = m1;
-            if (t + 2 < p.T) dst[2] = m2;
-            if (t + 3 < p.T) dst[3] = m3;
-          }
-        }
+        if (DQK <= 96) store_row_means(p, b, r, mu);   // pass 1 keeps the mean for pass 2
       }
       const f2 nmu = f2_make(-mu, -mu), rr = f2_make(rstd, rstd);
 #pragma unroll
@@ -353,6 +358,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           asm volatile("" ::: "memory");
         }
       }
+      // (d_qk = 128: after the rotation, whose registers it would crowd)
+      if (!QUANT && DQK > 96) store_row_means(p, b, r, mu);
       nbox = DQK / 32;
     } else {
       uint4 x[8];

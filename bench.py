@@ -71,7 +71,7 @@ def algorithmic_work(s: synth.Shape):
 KERNEL_SOURCES = {"bwd": "bwd.cu", "gemm": "gemm.cu", "quant": "quant.cu"}
 TRAFFIC = {
     "T": 49152,
-    "sources_sha256": {"bwd": "87c21ed8d25857686e2eb57923f434afaf9a423fa09913950e692f8a5c4c1b0e",
+    "sources_sha256": {"bwd": "1777f6c32b295348ded47b18b2f2b9085109759253829ccc4ab6266348dc5e1f",
                        "gemm": "c9de075080dc23a9d5634eeef7ed9d35df6004e98cdbcb2d6a71d068e2d946c9",
                        "quant": "270726eee5aada0c53740ecf87baf9304a5be421b85aac7ae31ba42d03c9339b"},
     # mean of two launches of the full-size step; dw_gemm: the GEMM and its

@@ -19,11 +19,13 @@
 // by TMA (the unit's [64 tokens x 32 cols] boxes, 64-byte swizzle) as soon
 // as the group has read a stage.  Two threads per token row: thread half h
 // owns the 8-column blocks (c / 8) % 2 == h of the row, which keeps each
-// rotation pair (i, i + d/2) in one thread; the row's mean(g_out * o) is one
-// shuffle between the two.  A thread's RoPE factors for a unit are loaded
-// before its stage is awaited, and the saved rstd and position one unit
-// ahead.  Pass 2 stages the codes of its unit (32-byte swizzle) and stores
-// them by TMA while the other group computes.
+// rotation pair (i, i + d/2) in one thread; pass 1 forms the row's
+// mean(g_out * o) with one shuffle between the two and stores it in the
+// workspace, and pass 2 reads it back instead of forming it again (the same
+// value, so the same dY).  A thread's RoPE factors for a unit are loaded
+// before its stage is awaited, and the saved rstd, position (and in pass 2
+// mean) one unit ahead.  Pass 2 stages the codes of its unit (32-byte
+// swizzle) and stores them by TMA while the other group computes.
 // Within a warp, lanes map to rows so that the 16-byte reads of a quarter
 // warp hit eight distinct 16-byte bank groups of the swizzled boxes.  In
 // pass 1 the group's threads meet only through mbarriers (a stage landed;
